@@ -1,0 +1,452 @@
+"""Benchmark: one MoE layer forward + backward through the grouped-GEMM path.
+
+A step is one pass of the whole hot path over one batch of synthetic input
+(configuration "mlp8": T=8192 tokens, hidden 4096, expert intermediate 14336
+(gate_up N = 28672), E=8 experts, top-2):
+    route          gg_route_hist_offsets   histogram, offsets, stable permutation
+    permute        gg_permute              X -> expert order (input of dW1)
+    GEMM1 fwd      gg_forward              permute_x (token gather fused)
+    GEMM2 fwd      gg_forward              permute_y (scatter to token order fused)
+    combine        gg_unpermute_combine    weighted top-k combine -> [T, hidden]
+    GEMM2 bwd      gg_backward_dX (permute_y), gg_backward_dW (permute_y)
+    GEMM1 bwd      gg_backward_dX (permute_x, + top-k token sum), gg_backward_dW
+The GEMM2 input stands in for act(GEMM1) (a seeded tensor), and the output
+gradients are seeded tensors; FLOPs counted are 2*R*N*K per GEMM pass (6
+passes), padding rows not counted.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gg|reference]
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs an independent
+replica of the layer on its own GPU (weak scaling, no collective on the data
+path); value = FLOPs of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "grouped-GEMM fwd+bwd TFLOP/s and % of bf16 tensor peak; permute GB/s vs HBM"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as fh:
+                d = json.load(fh)
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _peak_value(d, keys, default):
+    for k in keys:
+        v = d.get(k)
+        if isinstance(v, (int, float)) and v > 0:
+            return float(v)
+        if isinstance(v, dict):
+            for kk in ("value", "peak", "tflops", "gbs"):
+                if isinstance(v.get(kk), (int, float)):
+                    return float(v[kk])
+    return default
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _gemm_passes(cfg):
+    R, K, N1, I = cfg.R, cfg.K, cfg.N1, cfg.I
+    f1 = 2.0 * R * N1 * K
+    f2 = 2.0 * R * K * I
+    return {"fwd1": f1, "fwd2": f2, "dX2": f2, "dW2": f2, "dX1": f1, "dW1": f1}
+
+
+# --------------------------------------------------------------- CPU oracle --
+
+def oracle_sample(cfg, host, ro, rows_per_pass, rng):
+    """Time the oracle as it stands on a bounded sample of the step: a few
+    expert-order rows of every GEMM pass (plus the full route).  Returns
+    (seconds, flops, description)."""
+    from oracle import oracle as orc
+    t0 = time.perf_counter()
+    orc.route(host["ids"], cfg.T, cfg.topk, cfg.E)
+    flops = 0.0
+    R = cfg.R
+    rows = np.sort(rng.choice(R, size=rows_per_pass, replace=False)).astype(np.int64)
+    # GEMM1 forward (gather), GEMM2 forward (scatter)
+    orc.forward_rows(host["X"], host["W1"], ro["m_sizes"], ro["gather_idx"], host["w"], cfg.topk,
+                     1, 0, 0, rows)
+    flops += rows.size * 2.0 * cfg.N1 * cfg.K
+    orc.forward_rows(host["A2"], host["W2"], ro["m_sizes"], ro["gather_idx"], host["w"], cfg.topk,
+                     0, 1, 0, rows)
+    flops += rows.size * 2.0 * cfg.K * cfg.I
+    orc.backward_dX_rows(host["dY2"], host["W2"], ro["m_sizes"], ro["gather_idx"], 0, 1, rows)
+    flops += rows.size * 2.0 * cfg.K * cfg.I
+    orc.backward_dX_rows(host["dH"], host["W1"], ro["m_sizes"], ro["gather_idx"], 1, 0, rows)
+    flops += rows.size * 2.0 * cfg.N1 * cfg.K
+    # dW rows: row n of dW[e] reduces over all m_e rows of expert e
+    es = rng.integers(0, cfg.E, size=max(1, rows_per_pass // 4)).astype(np.int32)
+    es = np.array([e for e in es if ro["m_sizes"][e] > 0] or [int(np.argmax(ro["m_sizes"]))], np.int32)
+    ns2 = rng.integers(0, cfg.K, size=es.size).astype(np.int64)
+    orc.backward_dW_rows(host["A2"], host["dY2"], ro["m_sizes"], ro["gather_idx"], cfg.topk, 0, 1, es, ns2)
+    flops += float(sum(2.0 * ro["m_sizes"][e] * cfg.I for e in es))
+    ns1 = rng.integers(0, cfg.N1, size=es.size).astype(np.int64)
+    orc.backward_dW_rows(host["X"], host["dH"], ro["m_sizes"], ro["gather_idx"], cfg.topk, 1, 0, es, ns1)
+    flops += float(sum(2.0 * ro["m_sizes"][e] * cfg.K for e in es))
+    dt = time.perf_counter() - t0
+    desc = ("full route + %d expert-order rows of each forward and dX pass + %d rows of each dW "
+            "pass (oracle, fp64, OpenMP)" % (rows.size, es.size))
+    return dt, flops, desc
+
+
+def make_host(cfg):
+    from unpermute_route_hist_gb300 import synth
+    ids, w = synth.route_choices(cfg)
+    host = synth.moe_tensors(cfg)
+    host["ids"], host["w"] = ids, w
+    return host
+
+
+def run_reference(args, cfg):
+    """The reference arm: the CPU oracle as it stands, a bounded sample per step."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+    orc.build()
+    host = make_host(cfg)
+    ro = orc.route(host["ids"], cfg.T, cfg.topk, cfg.E)
+    rng = np.random.default_rng(1234)
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(cfg, host, ro, rows, rng)
+    times, flops, desc = [], 0.0, ""
+    for _ in range(args.steps):
+        dt, fl, desc = oracle_sample(cfg, host, ro, rows, rng)
+        times.append(dt)
+        flops += fl
+    total = sum(times)
+    value = flops / total / 1e12
+    cores = orc.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config_dict(cfg, ws),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config_dict(cfg, ws):
+    return {"workload": "MoE layer fwd+bwd, %s: T=%d, hidden K=%d, gate_up N=%d, down I=%d, E=%d, "
+                        "topk=%d, bf16, %s routing" % (cfg.name, cfg.T, cfg.K, cfg.N1, cfg.I, cfg.E,
+                                                       cfg.topk, cfg.routing),
+            "tokens_per_gpu": cfg.T, "experts": cfg.E, "topk": cfg.topk,
+            "parallelism": "replicas" if ws > 1 else "single",
+            "l2": "inputs larger than L2 (weights 2.6 GiB, activations > 1 GiB per step)"}
+
+
+# ----------------------------------------------------------------- GPU arm --
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], 0, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = max(mx, float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names[1:], parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_gg(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    import unpermute_route_hist_gb300 as gg
+    from unpermute_route_hist_gb300 import _lib
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    _lib.load()
+
+    host = make_host(cfg)
+    T, k, E, K, N1, I, R = cfg.T, cfg.topk, cfg.E, cfg.K, cfg.N1, cfg.I, cfg.R
+
+    def to_dev(u16):
+        return torch.from_numpy(u16.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def pinned(u16):
+        t = torch.from_numpy(u16.view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    W1, W2 = to_dev(host["W1"]), to_dev(host["W2"])
+    inputs_host = {"X": host["X"], "A2": host["A2"], "dY2": host["dY2"], "dH": host["dH"]}
+    d = {n: to_dev(v) for n, v in inputs_host.items()}
+    ids = torch.from_numpy(host["ids"]).to(dev)
+    wts = torch.from_numpy(host["w"]).to(dev)
+    bf = torch.bfloat16
+    o = {
+        "m_sizes": torch.empty(E, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+        "gather_idx": torch.empty(R, dtype=torch.int32, device=dev),
+        "row_id_map": torch.empty(R, dtype=torch.int32, device=dev),
+    }
+    ws_buf = torch.empty(gg.route_workspace_size(T, k, E), dtype=torch.uint8, device=dev)
+    Xp = torch.empty(R, K, dtype=bf, device=dev)
+    H = torch.empty(R, N1, dtype=bf, device=dev)
+    Y2 = torch.empty(R, K, dtype=bf, device=dev)
+    out = torch.empty(T, K, dtype=bf, device=dev)
+    dA2 = torch.empty(R, I, dtype=bf, device=dev)
+    dW2 = torch.empty(E, K, I, dtype=bf, device=dev)
+    dX1 = torch.empty(R, K, dtype=bf, device=dev)
+    dXt = torch.empty(T, K, dtype=bf, device=dev)
+    dW1 = torch.empty(E, N1, K, dtype=bf, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    passes = _gemm_passes(cfg)
+    step_flops = sum(passes.values())
+
+    ev_names = ["route", "permute", "fwd1", "fwd2", "combine", "dX2", "dW2", "dX1", "dW1"]
+
+    def step(src, evs=None):
+        def mark(i):
+            if evs is not None:
+                evs[i].record()
+        mark(0)
+        r = gg.route_hist_offsets(src["ids"], E, 0, workspace=ws_buf, status=status, outs=o)
+        mark(1)
+        gg.permute(src["X"], r["row_id_map"], k, out=Xp, status=status)
+        mark(2)
+        gg.forward(src["X"], W1, r["m_sizes"], r["gather_idx"], None, k, True, False, False, out=H,
+                   status=status)
+        mark(3)
+        gg.forward(src["A2"], W2, r["m_sizes"], r["gather_idx"], None, k, False, True, False, out=Y2,
+                   status=status)
+        mark(4)
+        gg.unpermute_combine(Y2, None, src["w"], T, k, out=out, status=status)
+        mark(5)
+        gg.backward_dX(src["dY2"], W2, r["m_sizes"], r["gather_idx"], T, k, False, True, out=dA2,
+                       status=status)
+        mark(6)
+        gg.backward_dW(src["A2"], src["dY2"], r["m_sizes"], r["gather_idx"], T, k, False, True,
+                       out=dW2, status=status)
+        mark(7)
+        gg.backward_dX(src["dH"], W1, r["m_sizes"], r["gather_idx"], T, k, True, False,
+                       token_sum=True, out=dX1, out_tok=dXt, status=status)
+        mark(8)
+        gg.backward_dW(Xp, src["dH"], r["m_sizes"], r["gather_idx"], T, k, False, False, out=dW1,
+                       status=status)
+        mark(9)
+
+    launches_per_step = 4 + 1 + 1 + 1 + 1 + 1 + 1 + 2 + 1  # route(4) permute fwd fwd combine dX dW dX(+sum) dW
+    src = dict(d, ids=ids, w=wts)
+    for _ in range(max(args.warmup, 3)):
+        step(src)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d: %s" % (int(status.item()),
+                                                      _lib.device_status_string(int(status.item()))))
+
+    # ---- timed region: inputs resident in HBM --------------------------------
+    stream = torch.cuda.current_stream(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ev_names) + 1)]
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(src, evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    per = {n: 0.0 for n in ev_names}
+    for s in range(args.steps):
+        for i, n in enumerate(ev_names):
+            per[n] += evs[s][i].elapsed_time(evs[s][i + 1])
+    per = {n: v / args.steps for n, v in per.items()}
+    if ws > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    value = step_flops * ws / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers ------------------
+    pin = {n: pinned(v) for n, v in inputs_host.items()}
+    pin_ids = torch.from_numpy(host["ids"]).pin_memory()
+    pin_w = torch.from_numpy(host["w"]).pin_memory()
+    res_host = torch.empty(T, K, dtype=bf).pin_memory()
+    res_host2 = torch.empty(T, K, dtype=bf).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin.values()) + pin_ids.numel() * 4 + pin_w.numel() * 4
+    d2h = 2 * T * K * 2
+    e_steps = max(2, min(args.steps, 5))
+
+    def e2e_step():
+        for n in pin:
+            d[n].copy_(pin[n], non_blocking=True)
+        ids.copy_(pin_ids, non_blocking=True)
+        wts.copy_(pin_w, non_blocking=True)
+        step(src)
+        res_host.copy_(out, non_blocking=True)
+        res_host2.copy_(dXt, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / e_steps
+    if ws > 1:
+        tt = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e_ms = float(tt.item())
+    e_value = step_flops * ws / (e_ms * 1e-3) / 1e12
+
+    # ---- HBM-bound movers: GB/s of the timed permute and combine --------------
+    perm_bytes = T * K * 2 + R * K * 2 + R * 4
+    comb_bytes = R * K * 2 + R * 4 + T * K * 2  # weights R*4 also read
+    comb_bytes += R * 4
+
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d after the timed region" % int(status.item()))
+
+    if rank == 0:
+        peaks, src_kind = _peaks()
+        tflops_sus = _peak_value(peaks, ["bf16_tflops_sustained", "bf16_tflops"], 1700.0)
+        hbm = _peak_value(peaks, ["hbm_gbs", "hbm_GBs", "hbm"], 6800.0)
+        dom = "fwd1"
+        achieved = passes[dom] / (per[dom] * 1e-3) / 1e12
+        gemm_ms = sum(per[n] for n in passes)
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": _config_dict(cfg, ws),
+            "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (GEMM1 forward, token gather)",
+                         "achieved": achieved, "peak": tflops_sus, "unit": "TFLOP/s",
+                         "frac": achieved / tflops_sus, "peak_source": src_kind + " bf16 sustained",
+                         "traffic": None},
+            "gemm": {"tflops_all_gemm_launches": sum(passes.values()) / (gemm_ms * 1e-3) / 1e12,
+                     "frac_of_peak": sum(passes.values()) / (gemm_ms * 1e-3) / 1e12 / tflops_sus,
+                     "ms": {n: per[n] for n in passes}},
+            "hbm_movers": {"permute_GBps": perm_bytes / (per["permute"] * 1e-3) / 1e9,
+                           "combine_GBps": comb_bytes / (per["combine"] * 1e-3) / 1e9,
+                           "peak_GBps": hbm, "peak_source": src_kind,
+                           "permute_frac": perm_bytes / (per["permute"] * 1e-3) / 1e9 / hbm,
+                           "combine_frac": comb_bytes / (per["combine"] * 1e-3) / 1e9 / hbm,
+                           "route_ms": per["route"]},
+            "e2e": {"value": e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline and ws == 1:
+            from oracle import oracle as orc
+            orc.build()
+            ro = orc.route(host["ids"], T, k, E)
+            rng = np.random.default_rng(99)
+            dt, fl, desc = oracle_sample(cfg, host, ro, args.ref_rows, rng)
+            line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s",
+                                    "cores": orc.num_threads(), "kind": "oracle", "sample": desc,
+                                    "seconds": dt}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gg", choices=["gg", "reference"])
+    ap.add_argument("--config", default="mlp8")
+    ap.add_argument("--ref-rows", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from unpermute_route_hist_gb300 import synth
+    cfg = synth.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_gg(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

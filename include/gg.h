@@ -1,0 +1,183 @@
+/*
+ * gg.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts grouped GEMM library.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - T = num_tokens, topk = experts per token, R = T * topk routed rows,
+ *    E = experts.  A "flat slot" f = t * topk + j names slot j of token t.
+ *    An "expert-order row" i lies in [offsets[e], offsets[e+1]) for its expert.
+ *  - bf16 tensors are passed as `gg_bf16*` (raw IEEE bfloat16 bits), row-major,
+ *    rows contiguous.  Weights W are (E, N, K) with K contiguous.
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless it
+ *    is documented otherwise.  The library allocates no device memory.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *    = the legacy default stream).  Inputs must stay valid until the stream
+ *    reaches the call.
+ *  - Return value: GG_OK (0), or a negative GG_ERR_* code for an error found
+ *    synchronously on the host (bad arguments, unsupported shape, launch
+ *    failure).  Nothing is launched when an error is returned.
+ *  - `status` (optional, may be NULL): a device int32 the kernels set, with an
+ *    atomic compare-and-swap from 0, to a GG_DEV_* code when they find bad
+ *    input data (an expert id out of range, a row index out of range) or a
+ *    bounded wait ran out.  The offending access is skipped, never performed.
+ *    The caller zeroes it and reads it after synchronising.
+ *  - Size rules (else GG_ERR_UNSUPPORTED): row widths K and N multiples of 8
+ *    (16-byte rows), every tensor pointer 16-byte aligned, E <= GG_MAX_EXPERTS,
+ *    topk <= GG_MAX_TOPK, R < 2^31.
+ *  - An empty problem (no rows or no output columns) returns GG_OK without a
+ *    launch; an empty reduction writes zeros.
+ *
+ * Sources cited below (page title, then section):
+ *  [U] unslothai--unsloth unsloth/kernels/moe/grouped_gemm/interface.py
+ *  [V] vllm third_party/triton_kernels/matmul_ogs.py
+ *  [W] VLA/wall_x/fusions/backend.py
+ */
+#ifndef GG_H
+#define GG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t gg_bf16;
+
+/* host-side return codes */
+#define GG_OK 0
+#define GG_ERR_INVALID_ARG (-1)
+#define GG_ERR_UNSUPPORTED (-2)
+#define GG_ERR_CUDA (-3)
+#define GG_ERR_WORKSPACE (-6)
+
+/* device status word codes */
+#define GG_DEV_OK 0
+#define GG_DEV_BAD_EXPERT_ID 1
+#define GG_DEV_BAD_ROW_INDEX 2
+#define GG_DEV_SIZES_MISMATCH 3
+#define GG_DEV_TIMEOUT 4
+
+#define GG_MAX_EXPERTS 2048
+#define GG_MAX_TOPK 64
+
+/* Human-readable text for a GG_* return code (static storage). */
+const char* gg_status_string(int code);
+/* Human-readable text for a GG_DEV_* device status code (static storage). */
+const char* gg_device_status_string(int code);
+/* Text of the last CUDA error seen by a host call on this thread. */
+const char* gg_last_cuda_error(void);
+
+/* ------------------------------------------------------------------ route --
+ * Routing metadata from the router's choices ([U] grouped_gemm_forward
+ * docstring: m_sizes = tokens per expert, gather_indices sliced by
+ * cumsum(m_sizes) gives each expert's token slots; [V] RoutingData.expt_hist,
+ * GatherIndx / ScatterIndx; [V] ragged-dw comment for the padded layout;
+ * [W] permute).
+ *
+ *  topk_ids       [T, topk] int32 expert id of each slot (must be in [0, E)).
+ *  pad_block      > 0: also write padded_offsets; <= 0: padded_offsets unused.
+ *  m_sizes        [E]   out: rows per expert.
+ *  offsets        [E+1] out: exclusive prefix of m_sizes, offsets[E] = R.
+ *  padded_offsets [E+1] out (or NULL): prefix of ceil(m_e/pad_block)*pad_block.
+ *  gather_idx     [R]   out: flat slot f held by expert-order row i; within an
+ *                       expert, slots ascend (stable order).
+ *  row_id_map     [R]   out (or NULL): inverse, row_id_map[gather_idx[i]] = i.
+ *  workspace      device scratch of at least gg_route_workspace_size() bytes,
+ *                 owned by the caller; contents need no initialisation and are
+ *                 garbage afterwards.  Too small -> GG_ERR_WORKSPACE.
+ * An id outside [0, E) sets GG_DEV_BAD_EXPERT_ID; that slot is not counted and
+ * gets no row (the outputs are then incomplete). */
+size_t gg_route_workspace_size(int64_t T, int topk, int E);
+int gg_route_hist_offsets(const int32_t* topk_ids, int64_t T, int topk, int E, int pad_block,
+                          int32_t* m_sizes, int32_t* offsets, int32_t* padded_offsets,
+                          int32_t* gather_idx, int32_t* row_id_map, void* workspace,
+                          size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ---------------------------------------------------------------- permute --
+ * Token rows into expert order ([W] permute; [U] permute_x): for every slot f
+ * of token t, Xp[row_id_map[f], :] = X[t, :].  Equivalently
+ * Xp[i, :] = X[gather_idx[i] / topk, :].  Bit-exact copy.
+ *  X [T, K] bf16, row_id_map [R] int32 (from gg_route_hist_offsets),
+ *  Xp [R, K] bf16 out.  A map entry outside [0, R) sets GG_DEV_BAD_ROW_INDEX. */
+int gg_permute(const gg_bf16* X, const int32_t* row_id_map, int64_t T, int topk, int64_t K,
+               gg_bf16* Xp, int32_t* status, void* stream);
+
+/* ------------------------------------------------------ unpermute-combine --
+ * Expert outputs back to token order, weighted combine over a token's slots
+ * ([W] unpermute: combine with routing probabilities; [V] matmul_ogs_torch:
+ * accumulate every slot of a token in fp32):
+ *   out[t, :] = bf16( sum_{j<topk} w[t*topk+j] * Y[row(t*topk+j), :] )
+ * summed in fp32 in j order.
+ *  Y [R, N] bf16; row_id_map [R] int32, or NULL when Y is already in
+ *  token-slot order (row(f) = f, e.g. after a forward with permute_y);
+ *  topk_w [T, topk] fp32, or NULL for unit weights; out [T, N] bf16.
+ * With row_id_map = NULL and topk_w = NULL this is the top-k sum of a
+ * token-slot-ordered tensor ([U] GroupedGemm.backward, the sum over topk). */
+int gg_unpermute_combine(const gg_bf16* Y, const int32_t* row_id_map, const float* topk_w,
+                         int64_t T, int topk, int64_t N, gg_bf16* out, int32_t* status,
+                         void* stream);
+
+/* ---------------------------------------------------------------- forward --
+ * Grouped GEMM forward ([U] grouped_gemm_forward; [V] matmul_ogs docstring:
+ * Y[idx_y(e)] = X[idx_x(e)] @ W[e]^T):
+ *   for every expert-order row i of expert e:
+ *     a   = X[gather_idx[i] / topk]  if permute_x  (X is [T, K])
+ *           X[i]                      otherwise    (X is [R, K], expert order)
+ *     y   = a @ W[e]^T                (fp32 accumulate)
+ *     y  *= topk_w[gather_idx[i]]     if fuse_mul_post (needs permute_y)
+ *     Y[gather_idx[i]] = bf16(y)      if permute_y (token-slot order)
+ *     Y[i]             = bf16(y)      otherwise
+ *  W [E, N, K] bf16; m_sizes [E] int32 with sum R; gather_idx [R] (needed when
+ *  a permute flag is set); topk_w [T, topk] fp32 (needed for fuse_mul_post);
+ *  Y [R, N] bf16 out.  permute_x and permute_y may be combined (gather on
+ *  load and scatter on store in one pass). */
+int gg_forward(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
+               const int32_t* gather_idx, const float* topk_w, int64_t T, int topk, int E,
+               int64_t N, int64_t K, int permute_x, int permute_y, int fuse_mul_post,
+               gg_bf16* Y, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------ backward dX --
+ * Gradient of the forward's input ([U] grouped_gemm_dX; GroupedGemm.backward):
+ *   for every expert-order row i of expert e:
+ *     g  = dY[gather_idx[i]] if permute_y else dY[i]     (dY is [R, N])
+ *     dx = g @ W[e]                                      (reduce over N)
+ *     dX[gather_idx[i]] = bf16(dx) if permute_x (token-slot order) else dX[i]
+ *  dX [R, K] bf16 out.  dX_tok [T, K] bf16 out or NULL: with permute_x, the
+ *  per-token sum over its topk slots of the stored bf16 dX rows (fp32 sum in
+ *  slot order).  dX_tok without permute_x -> GG_ERR_INVALID_ARG.  The flags
+ *  are those of the forward call being differentiated. */
+int gg_backward_dX(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes,
+                   const int32_t* gather_idx, int64_t T, int topk, int E, int64_t N, int64_t K,
+                   int permute_x, int permute_y, gg_bf16* dX, gg_bf16* dX_tok, int32_t* status,
+                   void* stream);
+
+/* ------------------------------------------------------------ backward dW --
+ * Gradient of the expert weights ([U] grouped_gemm_dW; [V] ragged-dw comment:
+ * the reduction dimension is each expert's own rows):
+ *   dW[e] = sum over expert-order rows i of e of  outer(g_i, a_i)   -> (N, K)
+ *     a_i = X[gather_idx[i] / topk] if permute_x else X[i]
+ *     g_i = dY[gather_idx[i]]       if permute_y else dY[i]
+ *  fp32 accumulate, bf16 out; an expert with no rows gets dW[e] = 0.
+ *  X [T, K] if permute_x else [R, K]; dY [R, N]; dW [E, N, K] bf16 out. */
+int gg_backward_dW(const gg_bf16* X, const gg_bf16* dY, const int32_t* m_sizes,
+                   const int32_t* gather_idx, int64_t T, int topk, int E, int64_t N, int64_t K,
+                   int permute_x, int permute_y, gg_bf16* dW, int32_t* status, void* stream);
+
+/* --------------------------------------------------------- dual asymmetric --
+ * Two experts' GEMMs with different row counts and output widths in one
+ * launch ([W] asym_dual_gmm_separated):  Y0 = op(X0) @ op(W0),
+ * Y1 = op(X1) @ op(W1), shared reduction length k.
+ *  trans_a = 0: X0 [m0, k], X1 [m1, k];  trans_a = 1: X0 [k, m0], X1 [k, m1].
+ *  trans_b = 0: W0 [k, n0], W1 [k, n1];  trans_b = 1: W0 [n0, k], W1 [n1, k].
+ *  Y0 [m0, n0], Y1 [m1, n1] bf16 out, fp32 accumulate.
+ *  m0, m1, n0, n1 and k must be multiples of 8 (16-byte rows either way). */
+int gg_dual_asym(const gg_bf16* X0, const gg_bf16* X1, const gg_bf16* W0, const gg_bf16* W1,
+                 gg_bf16* Y0, gg_bf16* Y1, int64_t m0, int64_t m1, int64_t k, int64_t n0,
+                 int64_t n1, int trans_a, int trans_b, int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GG_H */

@@ -96,6 +96,7 @@ int oracle_route(const int32_t* ids, int64_t T, int topk, int E, int pad_block,
                  int32_t* m_sizes, int32_t* offsets, int32_t* padded_offsets,
                  int32_t* gather_idx, int32_t* row_id_map) {
     int64_t R = T * (int64_t)topk;
+    if (E <= 0 || T < 0 || topk <= 0) return -1;
     for (int e = 0; e < E; ++e) m_sizes[e] = 0;
     for (int64_t f = 0; f < R; ++f) {
         int32_t e = ids[f];

@@ -1,0 +1,219 @@
+"""GPU parity at sizes the oracle finishes in seconds: every output element
+compared with the CPU oracle.  Input scales keep outputs O(1), as in the
+configs (the absolute 2e-2 bound presumes that).  Integer / index / copy outputs bit-exact;
+bf16-in/fp32-accumulate outputs within the benchmark spec's tolerance plus a tight
+elementwise bound.  Shapes span several 128x256 tiles with ragged tails,
+empty experts, and every permute/scale flag combination."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import unpermute_route_hist_gb300 as gg
+from oracle import oracle as orc
+from unpermute_route_hist_gb300 import synth
+
+from gpu_util import assert_close, dbf, df32, di32, hbf, status_of, status_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+
+
+def _ids(T, topk, E, seed, empty=()):
+    rng = np.random.default_rng(seed)
+    choices = [e for e in range(E) if e not in empty]
+    return rng.choice(choices, size=(T, topk)).astype(np.int32)
+
+
+def _route_gpu(ids, E, pad_block=0):
+    st = status_tensor()
+    r = gg.route_hist_offsets(di32(ids), E, pad_block, status=st)
+    assert status_of(st) == 0
+    return r
+
+
+# ------------------------------------------------------------------ route --
+
+@pytest.mark.parametrize("T,topk,E,seed,empty", [
+    (64, 2, 4, 0, ()), (1, 1, 1, 1, ()), (300, 3, 7, 2, (0, 5)), (1000, 8, 128, 3, (1, 2, 3)),
+    (257, 1, 2048, 4, ()), (4096, 4, 64, 5, ()), (999, 2, 1, 6, ()), (513, 2, 3, 7, (0, 1))])
+def test_route_bit_exact(T, topk, E, seed, empty):
+    ids = _ids(T, topk, E, seed, empty)
+    r = _route_gpu(ids, E, pad_block=128)
+    ro = orc.route(ids, T, topk, E, pad_block=128)
+    for k in ("m_sizes", "offsets", "padded_offsets", "gather_idx", "row_id_map"):
+        np.testing.assert_array_equal(r[k].cpu().numpy(), ro[k], err_msg=k)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mlp8", "fine128", "zipf64"])
+def test_route_configs_bit_exact(name):
+    cfg = synth.CONFIGS[name]
+    ids, _ = synth.route_choices(cfg)
+    r = _route_gpu(ids, cfg.E, pad_block=64)
+    ro = orc.route(ids, cfg.T, cfg.topk, cfg.E, pad_block=64)
+    for k in ("m_sizes", "offsets", "padded_offsets", "gather_idx", "row_id_map"):
+        np.testing.assert_array_equal(r[k].cpu().numpy(), ro[k], err_msg=k)
+
+
+def test_route_bad_expert_id_sets_status():
+    ids = _ids(100, 2, 4, 9)
+    ids[7, 1] = 4
+    ids[50, 0] = -3
+    st = status_tensor()
+    r = gg.route_hist_offsets(di32(ids), 4, status=st)
+    assert status_of(st) == 1  # GG_DEV_BAD_EXPERT_ID
+    # the good slots are still counted
+    good = ids[(ids >= 0) & (ids < 4)]
+    np.testing.assert_array_equal(r["m_sizes"].cpu().numpy(), np.bincount(good, minlength=4))
+
+
+# ---------------------------------------------------------------- permute --
+
+@pytest.mark.parametrize("T,topk,E,K", [(64, 2, 4, 128), (333, 8, 16, 8), (100, 1, 3, 4096),
+                                         (777, 4, 64, 264)])
+def test_permute_bit_exact(T, topk, E, K):
+    ids = _ids(T, topk, E, T + K)
+    ro = orc.route(ids, T, topk, E)
+    X = synth.normal_bf16(T, "px", (T, K), 1.0)
+    st = status_tensor()
+    Xp = gg.permute(dbf(X), di32(ro["row_id_map"]), topk, status=st)
+    assert status_of(st) == 0
+    np.testing.assert_array_equal(hbf(Xp), orc.permute(X, ro["gather_idx"], topk))
+
+
+def test_permute_bad_map_sets_status():
+    T, topk, K = 10, 2, 16
+    rim = np.arange(T * topk, dtype=np.int32)
+    rim[3] = T * topk + 5
+    st = status_tensor()
+    gg.permute(dbf(synth.normal_bf16(0, "x", (T, K), 1.0)), di32(rim), topk, status=st)
+    assert status_of(st) == 2  # GG_DEV_BAD_ROW_INDEX
+
+
+@pytest.mark.parametrize("T,topk,N,use_map,use_w", [(64, 2, 256, True, True), (300, 8, 40, True, False),
+                                                     (129, 4, 1032, False, True), (50, 1, 8, False, False)])
+def test_unpermute_combine(T, topk, N, use_map, use_w):
+    E = 5
+    ids = _ids(T, topk, E, N)
+    ro = orc.route(ids, T, topk, E)
+    Y = synth.normal_bf16(N, "cy", (T * topk, N), 0.25)
+    rng = np.random.default_rng(N)
+    w = rng.random((T, topk)).astype(np.float32) if use_w else None
+    rim = ro["row_id_map"] if use_map else None
+    st = status_tensor()
+    out = gg.unpermute_combine(dbf(Y), None if rim is None else di32(rim), None if w is None else df32(w),
+                               T, topk, status=st)
+    assert status_of(st) == 0
+    ref = orc.unpermute_combine(Y, rim, w, T, topk)
+    assert_close(hbf(out), ref, "combine")
+    # fp32 sum then one rounding: at most one bf16 rounding step from the exact sum
+    np.testing.assert_array_equal(np.abs(orc.widen_bf16(hbf(out)) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30, True)
+
+
+# ---------------------------------------------------------- grouped GEMMs --
+
+SHAPES = [
+    # T, topk, E, K, N, empty experts
+    (200, 2, 5, 320, 264, (3,)),
+    (64, 2, 4, 128, 256, ()),
+    (513, 4, 9, 136, 520, (0, 8)),
+]
+FWD_FLAGS = [(px, py, fm) for px, py, fm in itertools.product([0, 1], [0, 1], [0, 1]) if not (fm and not py)]
+
+
+def _problem(T, topk, E, K, N, empty, seed):
+    ids = _ids(T, topk, E, seed, empty)
+    rng = np.random.default_rng(seed)
+    _, w = synth.topk_softmax_route(rng.standard_normal((T, E)), topk)
+    ro = orc.route(ids, T, topk, E)
+    return ids, w, ro
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("px,py,fm", FWD_FLAGS)
+def test_forward(shape, px, py, fm):
+    T, topk, E, K, N, empty = shape
+    ids, w, ro = _problem(T, topk, E, K, N, empty, 11 + T)
+    R = T * topk
+    X = synth.normal_bf16(1, "fx", (T if px else R, K), 0.1)
+    W = synth.normal_bf16(2, "fw", (E, N, K), 0.1)
+    r = _route_gpu(ids, E)
+    st = status_tensor()
+    Y = gg.forward(dbf(X), dbf(W), r["m_sizes"], r["gather_idx"], df32(w), topk, bool(px), bool(py),
+                   bool(fm), status=st)
+    assert status_of(st) == 0
+    ref = orc.forward(X, W, ro["m_sizes"], ro["gather_idx"], w, T, topk, px, py, fm)
+    assert_close(hbf(Y), ref, "forward px=%d py=%d fm=%d" % (px, py, fm))
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("px,py", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_backward_dX(shape, px, py):
+    T, topk, E, K, N, empty = shape
+    ids, w, ro = _problem(T, topk, E, K, N, empty, 21 + T)
+    R = T * topk
+    dY = synth.normal_bf16(3, "dy", (R, N), 0.1)
+    W = synth.normal_bf16(4, "dw", (E, N, K), 0.1)
+    r = _route_gpu(ids, E)
+    st = status_tensor()
+    res = gg.backward_dX(dbf(dY), dbf(W), r["m_sizes"], r["gather_idx"], T, topk, bool(px), bool(py),
+                         token_sum=bool(px), status=st)
+    assert status_of(st) == 0
+    dX = res[0] if px else res
+    ref = orc.backward_dX(dY, W, ro["m_sizes"], ro["gather_idx"], T, topk, px, py)
+    assert_close(hbf(dX), ref, "dX px=%d py=%d" % (px, py))
+    if px:
+        assert_close(hbf(res[1]), orc.topk_sum(hbf(dX), T, topk), "dX token sum")
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("px,py", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_backward_dW(shape, px, py):
+    T, topk, E, K, N, empty = shape
+    ids, w, ro = _problem(T, topk, E, K, N, empty, 31 + T)
+    R = T * topk
+    X = synth.normal_bf16(5, "wx", (T if px else R, K), 0.1)
+    dY = synth.normal_bf16(6, "wy", (R, N), 0.1)
+    r = _route_gpu(ids, E)
+    st = status_tensor()
+    dW = gg.backward_dW(dbf(X), dbf(dY), r["m_sizes"], r["gather_idx"], T, topk, bool(px), bool(py),
+                        status=st)
+    assert status_of(st) == 0
+    ref = orc.backward_dW(X, dY, ro["m_sizes"], ro["gather_idx"], T, topk, px, py)
+    assert_close(hbf(dW), ref, "dW px=%d py=%d" % (px, py))
+    for e in empty:
+        assert (hbf(dW)[e] == 0).all()
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("dims", [(136, 72, 200, 264, 512), (512, 256, 1024, 2048, 4096), (8, 0, 64, 8, 16)])
+def test_dual_asym(ta, tb, dims):
+    m0, m1, k, n0, n1 = dims
+    cfg = synth.DualConfig(m0=m0, m1=m1, k=k, n0=n0, n1=n1, seed=7)
+    d = synth.dual_tensors(cfg, bool(ta), bool(tb))
+    st = status_tensor()
+    Y0, Y1 = gg.dual_asym(dbf(d["X0"]), dbf(d["X1"]), dbf(d["W0"]), dbf(d["W1"]), bool(ta), bool(tb),
+                          status=st)
+    assert status_of(st) == 0
+    R0, R1 = orc.dual_asym(d["X0"], d["X1"], d["W0"], d["W1"], bool(ta), bool(tb))
+    assert_close(hbf(Y0), R0, "dual Y0")
+    assert_close(hbf(Y1), R1, "dual Y1")
+
+
+def test_forward_bad_sizes_sets_status():
+    T, topk, E, K, N = 16, 2, 3, 64, 64
+    ids = _ids(T, topk, E, 1)
+    r = _route_gpu(ids, E)
+    m = r["m_sizes"].clone()
+    m[0] += 5  # no longer sums to T*topk
+    st = status_tensor()
+    X = dbf(synth.normal_bf16(0, "x", (T * topk, K), 1.0))
+    W = dbf(synth.normal_bf16(0, "w", (E, N, K), 1.0))
+    gg.forward(X, W, m, r["gather_idx"], None, topk, status=st)
+    assert status_of(st) == 3  # GG_DEV_SIZES_MISMATCH

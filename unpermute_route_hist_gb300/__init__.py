@@ -1,0 +1,12 @@
+"""GB300-native (sm_103a) Mixture-of-Experts grouped (ragged) GEMM.
+
+The computation lives in ``lib/libgg.so`` (C ABI in ``include/gg.h``); this
+package only loads it (``_lib``), marshals torch tensors into it (``api``)
+and provides seeded synthetic inputs (``synth``).
+"""
+from . import api  # noqa: F401
+from .api import (backward_dW, backward_dX, dual_asym, forward, permute,  # noqa: F401
+                  route_hist_offsets, route_workspace_size, unpermute_combine)
+
+__all__ = ["route_hist_offsets", "route_workspace_size", "permute", "unpermute_combine", "forward",
+           "backward_dX", "backward_dW", "dual_asym"]

@@ -1,0 +1,173 @@
+"""Python binding of the C ABI with the same names (minus the ``gg_`` prefix).
+
+Argument marshalling only: torch CUDA tensors provide device memory and the
+current stream; every step of the computation runs in libgg.so's kernels.
+Outputs may be passed in (``out=``) or are allocated here with ``torch.empty``.
+bf16 tensors are ``torch.bfloat16``; index tensors ``torch.int32``; routing
+weights ``torch.float32``.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import GGError  # noqa: F401  (re-export)
+
+
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device=None):
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need(t, dtype, name, shape=None):
+    if t is None:
+        raise ValueError("%s is required" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    return t
+
+
+def _opt(t, dtype, name, shape=None):
+    return None if t is None else _need(t, dtype, name, shape)
+
+
+def _out(out, shape, dtype, device, name):
+    if out is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    return _need(out, dtype, name, shape)
+
+
+def route_workspace_size(T: int, topk: int, E: int) -> int:
+    return int(_lib.load().gg_route_workspace_size(T, topk, E))
+
+
+def route_hist_offsets(topk_ids, E: int, pad_block: int = 0, *, workspace=None, status=None,
+                       row_id_map: bool = True, outs: dict | None = None) -> dict:
+    """m_sizes, offsets, padded_offsets (pad_block > 0), gather_idx, row_id_map."""
+    T, topk = topk_ids.shape
+    _need(topk_ids, torch.int32, "topk_ids")
+    dev = topk_ids.device
+    R = T * topk
+    o = dict(outs or {})
+    m = _out(o.get("m_sizes"), (E,), torch.int32, dev, "m_sizes")
+    off = _out(o.get("offsets"), (E + 1,), torch.int32, dev, "offsets")
+    poff = _out(o.get("padded_offsets"), (E + 1,), torch.int32, dev, "padded_offsets") if pad_block > 0 else None
+    g = _out(o.get("gather_idx"), (R,), torch.int32, dev, "gather_idx")
+    rim = _out(o.get("row_id_map"), (R,), torch.int32, dev, "row_id_map") if row_id_map else None
+    need = route_workspace_size(T, topk, E)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    rc = _lib.load().gg_route_hist_offsets(_p(topk_ids), T, topk, E, pad_block, _p(m), _p(off),
+                                           _p(poff), _p(g), _p(rim), _p(workspace),
+                                           workspace.numel() * workspace.element_size(), _p(status),
+                                           _stream(dev))
+    _lib.check("gg_route_hist_offsets", rc)
+    return dict(m_sizes=m, offsets=off, padded_offsets=poff, gather_idx=g, row_id_map=rim)
+
+
+def permute(X, row_id_map, topk: int, *, out=None, status=None):
+    _need(X, torch.bfloat16, "X")
+    T, K = X.shape
+    _need(row_id_map, torch.int32, "row_id_map", (T * topk,))
+    Xp = _out(out, (T * topk, K), torch.bfloat16, X.device, "out")
+    rc = _lib.load().gg_permute(_p(X), _p(row_id_map), T, topk, K, _p(Xp), _p(status), _stream(X.device))
+    _lib.check("gg_permute", rc)
+    return Xp
+
+
+def unpermute_combine(Y, row_id_map, topk_w, T: int, topk: int, *, out=None, status=None):
+    _need(Y, torch.bfloat16, "Y", (T * topk, Y.shape[1]))
+    N = Y.shape[1]
+    _opt(row_id_map, torch.int32, "row_id_map", (T * topk,))
+    _opt(topk_w, torch.float32, "topk_w")
+    if topk_w is not None and topk_w.numel() != T * topk:
+        raise ValueError("topk_w must have T*topk elements")
+    o = _out(out, (T, N), torch.bfloat16, Y.device, "out")
+    rc = _lib.load().gg_unpermute_combine(_p(Y), _p(row_id_map), _p(topk_w), T, topk, N, _p(o),
+                                          _p(status), _stream(Y.device))
+    _lib.check("gg_unpermute_combine", rc)
+    return o
+
+
+def forward(X, W, m_sizes, gather_idx, topk_w, topk: int, permute_x=False, permute_y=False,
+            fuse_mul_post=False, *, out=None, status=None):
+    _need(X, torch.bfloat16, "X")
+    _need(W, torch.bfloat16, "W")
+    E, N, K = W.shape
+    _need(m_sizes, torch.int32, "m_sizes", (E,))
+    rows = X.shape[0]
+    T = rows if permute_x else rows // topk
+    R = T * topk
+    if not permute_x and rows != R:
+        raise ValueError("X must have T*topk rows without permute_x")
+    _opt(gather_idx, torch.int32, "gather_idx", (R,))
+    _opt(topk_w, torch.float32, "topk_w")
+    Y = _out(out, (R, N), torch.bfloat16, X.device, "out")
+    rc = _lib.load().gg_forward(_p(X), _p(W), _p(m_sizes), _p(gather_idx), _p(topk_w), T, topk, E, N,
+                                K, int(permute_x), int(permute_y), int(fuse_mul_post), _p(Y),
+                                _p(status), _stream(X.device))
+    _lib.check("gg_forward", rc)
+    return Y
+
+
+def backward_dX(dY, W, m_sizes, gather_idx, T: int, topk: int, permute_x=False, permute_y=False,
+                *, token_sum=False, out=None, out_tok=None, status=None):
+    _need(dY, torch.bfloat16, "dY")
+    _need(W, torch.bfloat16, "W")
+    E, N, K = W.shape
+    R = T * topk
+    _need(dY, torch.bfloat16, "dY", (R, N))
+    _need(m_sizes, torch.int32, "m_sizes", (E,))
+    _opt(gather_idx, torch.int32, "gather_idx", (R,))
+    dX = _out(out, (R, K), torch.bfloat16, dY.device, "out")
+    dXt = _out(out_tok, (T, K), torch.bfloat16, dY.device, "out_tok") if token_sum else None
+    rc = _lib.load().gg_backward_dX(_p(dY), _p(W), _p(m_sizes), _p(gather_idx), T, topk, E, N, K,
+                                    int(permute_x), int(permute_y), _p(dX), _p(dXt), _p(status),
+                                    _stream(dY.device))
+    _lib.check("gg_backward_dX", rc)
+    return (dX, dXt) if token_sum else dX
+
+
+def backward_dW(X, dY, m_sizes, gather_idx, T: int, topk: int, permute_x=False, permute_y=False,
+                *, out=None, status=None):
+    _need(X, torch.bfloat16, "X")
+    _need(dY, torch.bfloat16, "dY")
+    E = m_sizes.shape[0]
+    _need(m_sizes, torch.int32, "m_sizes", (E,))
+    R = T * topk
+    K = X.shape[1]
+    N = dY.shape[1]
+    if X.shape[0] != (T if permute_x else R) or dY.shape[0] != R:
+        raise ValueError("X must have T (permute_x) or T*topk rows; dY T*topk rows")
+    _opt(gather_idx, torch.int32, "gather_idx", (R,))
+    dW = _out(out, (E, N, K), torch.bfloat16, X.device, "out")
+    rc = _lib.load().gg_backward_dW(_p(X), _p(dY), _p(m_sizes), _p(gather_idx), T, topk, E, N, K,
+                                    int(permute_x), int(permute_y), _p(dW), _p(status),
+                                    _stream(X.device))
+    _lib.check("gg_backward_dW", rc)
+    return dW
+
+
+def dual_asym(X0, X1, W0, W1, trans_a=False, trans_b=False, *, out0=None, out1=None, status=None):
+    for t, n in ((X0, "X0"), (X1, "X1"), (W0, "W0"), (W1, "W1")):
+        _need(t, torch.bfloat16, n)
+    k = X0.shape[0] if trans_a else X0.shape[1]
+    m0 = X0.shape[1] if trans_a else X0.shape[0]
+    m1 = X1.shape[1] if trans_a else X1.shape[0]
+    n0 = W0.shape[0] if trans_b else W0.shape[1]
+    n1 = W1.shape[0] if trans_b else W1.shape[1]
+    Y0 = _out(out0, (m0, n0), torch.bfloat16, X0.device, "out0")
+    Y1 = _out(out1, (m1, n1), torch.bfloat16, X0.device, "out1")
+    rc = _lib.load().gg_dual_asym(_p(X0), _p(X1), _p(W0), _p(W1), _p(Y0), _p(Y1), m0, m1, k, n0, n1,
+                                  int(trans_a), int(trans_b), _p(status), _stream(X0.device))
+    _lib.check("gg_dual_asym", rc)
+    return Y0, Y1

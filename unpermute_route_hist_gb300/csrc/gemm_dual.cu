@@ -1,0 +1,64 @@
+// gemm_dual.cu -- two experts' GEMMs with different row counts and output
+// widths, one launch (backend.py, asym_dual_gmm_separated).  The two problems'
+// tiles form one list for the persistent engine; each problem has its own pair
+// of tensor maps.  trans_a stores the inputs (k, m); trans_b stores the
+// weights (n, k) -- which decides whether each operand tile is K- or MN-major.
+#include "gemm_engine.cuh"
+
+using namespace gg;
+
+namespace {
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}
+
+extern "C" int gg_dual_asym(const gg_bf16* X0, const gg_bf16* X1, const gg_bf16* W0,
+                            const gg_bf16* W1, gg_bf16* Y0, gg_bf16* Y1, int64_t m0, int64_t m1,
+                            int64_t k, int64_t n0, int64_t n1, int trans_a, int trans_b,
+                            int32_t* status, void* stream) {
+    if (m0 < 0 || m1 < 0 || k < 0 || n0 < 0 || n1 < 0) return GG_ERR_INVALID_ARG;
+    if (m0 % 8 || m1 % 8 || k % 8 || n0 % 8 || n1 % 8) return GG_ERR_UNSUPPORTED;
+    const int64_t lim = int64_t(1) << 31;
+    if (m0 >= lim || m1 >= lim || k >= lim || n0 >= lim || n1 >= lim) return GG_ERR_UNSUPPORTED;
+    const bool e0 = m0 == 0 || n0 == 0, e1 = m1 == 0 || n1 == 0;
+    if (e0 && e1) return GG_OK;
+    if ((!e0 && (!X0 || !W0 || !Y0)) || (!e1 && (!X1 || !W1 || !Y1))) return GG_ERR_INVALID_ARG;
+    if ((!e0 && (!al16(X0) || !al16(W0) || !al16(Y0))) || (!e1 && (!al16(X1) || !al16(W1) || !al16(Y1))))
+        return GG_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (k == 0) {
+        cudaError_t e = cudaSuccess;
+        if (!e0) e = cudaMemsetAsync(Y0, 0, static_cast<size_t>(m0 * n0) * 2, st);
+        if (e == cudaSuccess && !e1) e = cudaMemsetAsync(Y1, 0, static_cast<size_t>(m1 * n1) * 2, st);
+        if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+        return GG_OK;
+    }
+    GemmParams p{};
+    p.E = 2;
+    p.Kred = static_cast<int>(k);
+    p.status = status;
+    p.dual[0] = DualProblem{e0 ? 0 : static_cast<int>(m0), e0 ? 0 : static_cast<int>(n0), Y0, n0};
+    p.dual[1] = DualProblem{e1 ? 0 : static_cast<int>(m1), e1 ? 0 : static_cast<int>(n1), Y1, n1};
+    CUtensorMap mA[2], mB[2];
+    const gg_bf16* Xs[2] = {X0, X1};
+    const gg_bf16* Ws[2] = {W0, W1};
+    const int64_t ms[2] = {m0, m1}, ns[2] = {n0, n1};
+    for (int q = 0; q < 2; ++q) {
+        const int src = (q == 0 ? e0 : e1) ? 1 - q : q;  // an empty problem borrows the other's maps
+        bool ok;
+        if (trans_a) ok = encode_map_2d(&mA[q], Xs[src], ms[src], k, ms[src], 64, kBK);
+        else ok = encode_map_2d(&mA[q], Xs[src], k, ms[src], k, kBK, kBM);
+        if (!ok) return GG_ERR_CUDA;
+        if (trans_b) ok = encode_map_2d(&mB[q], Ws[src], k, ns[src], k, kBK, kBN);
+        else ok = encode_map_2d(&mB[q], Ws[src], ns[src], k, ns[src], 64, kBK);
+        if (!ok) return GG_ERR_CUDA;
+    }
+    const int64_t bound = ((m0 + kBM - 1) / kBM) * ((n0 + kBN - 1) / kBN) +
+                          ((m1 + kBM - 1) / kBM) * ((n1 + kBN - 1) / kBN);
+    if (trans_a && trans_b)
+        return launch_gemm<KIND_DUAL, true, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
+    if (trans_a)
+        return launch_gemm<KIND_DUAL, true, true, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
+    if (trans_b)
+        return launch_gemm<KIND_DUAL, false, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
+    return launch_gemm<KIND_DUAL, false, true, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
+}

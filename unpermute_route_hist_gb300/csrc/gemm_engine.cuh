@@ -1,0 +1,648 @@
+// gemm_engine.cuh -- persistent, warp-specialised grouped GEMM on tcgen05.
+//
+// One kernel template serves every grouped contraction of the MoE path:
+//   forward  Y_e  = A_e  . W[e]^T    ragged M (each expert's rows), K-major A, B
+//   dX       dX_e = dY_e . W[e]      ragged M, K-major A, MN-major B (W read along N)
+//   dW       dW_e = dY_e^T . X_e     ragged reduction (each expert's rows),
+//                                    MN-major A and B
+//   dual     Y_p  = op(X_p) . op(W_p), p = 0, 1, one launch
+// (interface.py: grouped_gemm_forward / _dX / _dW; matmul_ogs.py: the ragged
+// dw comment; backend.py: asym_dual_gmm_separated.)
+//
+// Tile: 128 x 256 output, reduction blocks of 64, 4-stage shared-memory ring,
+// fp32 accumulators in tensor memory (two 256-column buffers so the epilogue
+// of one tile overlaps the main loop of the next).  Warp roles:
+//   warp 0      tile scheduler + TMA producer (lane 0) for dense operands
+//   warp 1      TMEM allocation + MMA issue (lane 0); zeroes ragged tails
+//   warps 2-5   epilogue: TMEM -> registers -> scale -> bf16 -> global rows
+//   warps 6-9   (only with a gathered operand) cp.async row-gather producers
+// Every role walks the same static tile list (tile = blockIdx.x + j*gridDim.x),
+// decoded from m_sizes in shared memory, so no role sends tile ids to another.
+//
+// Shared-memory operand layouts are the tcgen05 canonical 128-byte-swizzle
+// layouts: K-major tiles are rows of 64 bf16 (128 B), 8-row atoms of 1 KB;
+// MN-major tiles are 64-element MN chunks, each BK reduction rows of 128 B.
+// TMA with 128-byte swizzle writes exactly these; the gather producers write
+// the same swizzle by hand (16-byte chunk c of row r goes to c ^ (r & 7)).
+#pragma once
+
+#include "common.cuh"
+
+namespace gg {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;  // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators
+constexpr int kGroupM = 16;             // m-tiles per raster group (L2 reuse)
+constexpr int kGatherWarps = 4;
+constexpr int kGatherDepth = 2;         // cp.async stages in flight per thread
+
+enum GemmKind { KIND_RAGGED_M = 0, KIND_RAGGED_K = 1, KIND_DUAL = 2 };
+// Row index of a gathered operand row for expert-order row i.
+enum RowMode { ROW_DIRECT = 0, ROW_TOKEN = 1 /* gather_idx[i] / topk */, ROW_SLOT = 2 /* gather_idx[i] */ };
+
+struct GatherSrc {
+    const uint16_t* ptr;  // base of the source matrix
+    int64_t ld;           // elements between consecutive source rows
+    int64_t rows;         // number of source rows (bounds check)
+    int64_t cols;         // number of valid columns (MN extent or reduction extent)
+    int row_mode;
+};
+
+struct DualProblem {
+    int m, n;
+    uint16_t* out;
+    int64_t ld_out;
+};
+
+struct GemmParams {
+    int E, topk;
+    int64_t R;
+    int M;     // KIND_RAGGED_K: rows of each dW[e]
+    int N;     // output columns (per problem for dual: see dual[])
+    int Kred;  // reduction length (RAGGED_M, DUAL)
+    const int32_t* m_sizes;
+    const int32_t* gather_idx;
+    GatherSrc ga, gb;        // gathered A / B sources (when gathered)
+    uint16_t* out;
+    int64_t ld_out;
+    int scatter_out;         // RAGGED_M: store row gather_idx[i] instead of i
+    const float* scale;      // RAGGED_M: multiply row i by scale[gather_idx[i]]
+    DualProblem dual[2];
+    int32_t* status;
+};
+
+struct TileInfo {
+    int e;          // expert (problem index for dual)
+    int64_t row0;   // first output row: expert-order row (RAGGED_M), dW row, dual row
+    int rows;       // valid output rows in the tile
+    int n0;         // first output column
+    int64_t red0;   // first reduction row (RAGGED_K), else 0
+    int red_len;    // reduction length of the tile
+    int nkb;        // reduction blocks
+};
+
+struct SharedCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int bad_sizes;
+    int64_t total_tiles;
+};
+
+template <int KIND>
+__device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
+                                                const int32_t* s_off, const int32_t* s_tp) {
+    TileInfo ti;
+    if (KIND == KIND_RAGGED_M) {
+        const int nt_total = (p.N + kBN - 1) / kBN;
+        const int mt_total = s_tp[p.E];
+        const int64_t per_group = static_cast<int64_t>(kGroupM) * nt_total;
+        const int group = static_cast<int>(t / per_group);
+        const int first = group * kGroupM;
+        const int gsize = min(mt_total - first, kGroupM);
+        const int loc = static_cast<int>(t - group * per_group);
+        const int mt = first + loc % gsize;
+        const int nt = loc / gsize;
+        // largest e with s_tp[e] <= mt
+        int lo = 0, hi = p.E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_tp[mid] <= mt) lo = mid; else hi = mid - 1;
+        }
+        const int e = lo;
+        const int lmt = mt - s_tp[e];
+        const int me = s_off[e + 1] - s_off[e];
+        ti.e = e;
+        ti.row0 = static_cast<int64_t>(s_off[e]) + static_cast<int64_t>(lmt) * kBM;
+        ti.rows = min(kBM, me - lmt * kBM);
+        ti.n0 = nt * kBN;
+        ti.red0 = 0;
+        ti.red_len = p.Kred;
+    } else if (KIND == KIND_RAGGED_K) {
+        const int mt_per = (p.M + kBM - 1) / kBM;
+        const int nt_per = (p.N + kBN - 1) / kBN;
+        const int64_t per_e = static_cast<int64_t>(mt_per) * nt_per;
+        const int e = static_cast<int>(t / per_e);
+        const int loc = static_cast<int>(t - e * per_e);
+        const int mt = loc % mt_per, nt = loc / mt_per;
+        ti.e = e;
+        ti.row0 = static_cast<int64_t>(mt) * kBM;
+        ti.rows = min(kBM, p.M - mt * kBM);
+        ti.n0 = nt * kBN;
+        ti.red0 = s_off[e];
+        ti.red_len = s_off[e + 1] - s_off[e];
+    } else {
+        const int mt0 = (p.dual[0].m + kBM - 1) / kBM;
+        const int64_t tiles0 = static_cast<int64_t>(mt0) * ((p.dual[0].n + kBN - 1) / kBN);
+        const int q = t < tiles0 ? 0 : 1;
+        const int64_t lt = q == 0 ? t : t - tiles0;
+        const int mtq = (p.dual[q].m + kBM - 1) / kBM;
+        const int mt = static_cast<int>(lt % mtq), nt = static_cast<int>(lt / mtq);
+        ti.e = q;
+        ti.row0 = static_cast<int64_t>(mt) * kBM;
+        ti.rows = min(kBM, p.dual[q].m - mt * kBM);
+        ti.n0 = nt * kBN;
+        ti.red0 = 0;
+        ti.red_len = p.Kred;
+    }
+    ti.nkb = (ti.red_len + kBK - 1) / kBK;
+    return ti;
+}
+
+template <int KIND>
+__device__ __forceinline__ int tile_cols(const GemmParams& p, int e) {
+    return KIND == KIND_DUAL ? p.dual[e].n : p.N;
+}
+
+// Source row of a gathered operand for expert-order row i; -1 if out of range.
+__device__ __forceinline__ int64_t gather_row(const GemmParams& p, const GatherSrc& g, int64_t i) {
+    int64_t r;
+    if (g.row_mode == ROW_DIRECT) {
+        r = i;
+    } else {
+        const int32_t f = p.gather_idx[i];
+        r = g.row_mode == ROW_TOKEN ? static_cast<int64_t>(f) / p.topk : static_cast<int64_t>(f);
+    }
+    if (r < 0 || r >= g.rows) {
+        set_status(p.status, GG_DEV_BAD_ROW_INDEX);
+        return -1;
+    }
+    return r;
+}
+
+template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER>
+struct GemmTraits {
+    static constexpr bool kAnyGather = A_GATHER || B_GATHER;
+    static constexpr int kThreads = 32 * (6 + (kAnyGather ? kGatherWarps : 0));
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+    static constexpr uint32_t kTmaBytes = (A_GATHER ? 0u : kABytes) + (B_GATHER ? 0u : kBBytes);
+    static constexpr uint32_t kFullCount = 1 + (kAnyGather ? kGatherWarps * 32 : 0);
+};
+
+__host__ __device__ constexpr size_t gemm_smem_bytes(int E) {
+    return 1024 /* alignment slack */ + static_cast<size_t>(kStages) * kStageBytes +
+           sizeof(SharedCtl) + 2 * static_cast<size_t>(E + 1) * sizeof(int32_t) + 16;
+}
+
+// Shared-memory descriptor of k-step `ks` (16 reduction elements) of an operand tile.
+template <bool MN_MAJOR>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t tile_addr, int ks) {
+    if (MN_MAJOR) {
+        // MN chunks of 64 elements are kBK*128 bytes apart (leading offset);
+        // 8-row reduction groups are 1 KB apart (stride offset); a k-step is
+        // 16 reduction rows = 2 KB further.
+        return smem_desc_sw128(tile_addr + ks * 2048, kBK * 128, 1024);
+    } else {
+        // rows of 128 B, 8-row atoms 1 KB apart; a k-step is 32 B along the row.
+        return smem_desc_sw128(tile_addr + ks * 32, 16, 1024);
+    }
+}
+
+template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER>
+__global__ void __launch_bounds__((GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER>::kThreads), 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                    const GemmParams p) {
+    using Tr = GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t* stage_base = smem;
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kStages * kStageBytes);
+    int32_t* s_off = reinterpret_cast<int32_t*>(ctl + 1);
+    int32_t* s_tp = s_off + (p.E + 1);
+
+    const int warp = warp_id(), lane = lane_id();
+    volatile int* abort_flag = &ctl->abort_flag;
+
+    // ---------------------------------------------------------- prologue --
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ctl->full[s], Tr::kFullCount);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->tmem_full[b], 1);
+            mbar_init(&ctl->tmem_empty[b], 4);
+        }
+        mbar_init(&ctl->drain, 1);
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA0);
+        tma_prefetch_desc(&tmB0);
+        if (KIND == KIND_DUAL) {
+            tma_prefetch_desc(&tmA1);
+            tma_prefetch_desc(&tmB1);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 2) {
+        // Row offsets and (RAGGED_M) m-tile prefix of the experts: one warp,
+        // each lane scans a contiguous segment, then a warp scan of the sums.
+        int64_t total_tiles = 0;
+        int bad = 0;
+        if (KIND == KIND_DUAL) {
+            const int64_t t0 = static_cast<int64_t>((p.dual[0].m + kBM - 1) / kBM) * ((p.dual[0].n + kBN - 1) / kBN);
+            const int64_t t1 = static_cast<int64_t>((p.dual[1].m + kBM - 1) / kBM) * ((p.dual[1].n + kBN - 1) / kBN);
+            total_tiles = t0 + t1;
+        } else {
+            const int seg = (p.E + 31) / 32;
+            const int e_lo = min(p.E, lane * seg), e_hi = min(p.E, e_lo + seg);
+            int64_t rsum = 0;
+            int tsum = 0;
+            for (int e = e_lo; e < e_hi; ++e) {
+                const int m = p.m_sizes[e];
+                if (m < 0) bad = 1;
+                rsum += m > 0 ? m : 0;
+                tsum += m > 0 ? (m + kBM - 1) / kBM : 0;
+            }
+            int64_t rx = rsum;
+            int tx = tsum;
+            for (int d = 1; d < 32; d <<= 1) {
+                const int64_t ry = __shfl_up_sync(0xffffffffu, rx, d);
+                const int ty = __shfl_up_sync(0xffffffffu, tx, d);
+                if (lane >= d) { rx += ry; tx += ty; }
+            }
+            int64_t rrun = rx - rsum;
+            int trun = tx - tsum;
+            for (int e = e_lo; e < e_hi; ++e) {
+                const int m = max(p.m_sizes[e], 0);
+                s_off[e] = static_cast<int32_t>(rrun);
+                s_tp[e] = trun;
+                rrun += m;
+                trun += (m + kBM - 1) / kBM;
+            }
+            const int64_t rtot = __shfl_sync(0xffffffffu, rx, 31);
+            const int ttot = __shfl_sync(0xffffffffu, tx, 31);
+            bad = __any_sync(0xffffffffu, bad);
+            if (rtot != p.R) bad = 1;
+            if (lane == 0) {
+                s_off[p.E] = static_cast<int32_t>(rtot);
+                s_tp[p.E] = ttot;
+            }
+            if (KIND == KIND_RAGGED_M) {
+                total_tiles = static_cast<int64_t>(ttot) * ((p.N + kBN - 1) / kBN);
+            } else {
+                total_tiles = static_cast<int64_t>(p.E) * ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
+            }
+        }
+        if (lane == 0) {
+            ctl->bad_sizes = bad;
+            ctl->total_tiles = bad ? 0 : total_tiles;
+            if (bad && blockIdx.x == 0) set_status(p.status, GG_DEV_SIZES_MISMATCH);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const int64_t total_tiles = ctl->total_tiles;
+    const uint32_t stage0 = smem_u32(stage_base);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                const TileInfo ti = decode_tile<KIND>(t, p, s_off, s_tp);
+                const CUtensorMap* mA = (KIND == KIND_DUAL && ti.e == 1) ? &tmA1 : &tmA0;
+                const CUtensorMap* mB = (KIND == KIND_DUAL && ti.e == 1) ? &tmB1 : &tmB0;
+                for (int kb = 0; kb < ti.nkb; ++kb) {
+                    if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    uint8_t* sA = stage_base + stage * kStageBytes;
+                    uint8_t* sB = sA + kABytes;
+                    if (Tr::kTmaBytes) mbar_arrive_expect_tx(&ctl->full[stage], Tr::kTmaBytes);
+                    else mbar_arrive(&ctl->full[stage]);
+                    const int32_t red = static_cast<int32_t>(ti.red0 + static_cast<int64_t>(kb) * kBK);
+                    if (!A_GATHER) {
+                        if (!A_MN) {
+                            tma_load_2d(sA, mA, &ctl->full[stage], red, static_cast<int32_t>(ti.row0));
+                        } else {
+#pragma unroll
+                            for (int cc = 0; cc < kBM / 64; ++cc)
+                                tma_load_2d(sA + cc * kBK * 128, mA, &ctl->full[stage],
+                                            static_cast<int32_t>(ti.row0) + cc * 64, red);
+                        }
+                    }
+                    if (!B_GATHER) {
+                        if (!B_MN) {
+                            if (KIND == KIND_RAGGED_M)
+                                tma_load_3d(sB, mB, &ctl->full[stage], red, ti.n0, ti.e);
+                            else
+                                tma_load_2d(sB, mB, &ctl->full[stage], red, ti.n0);
+                        } else {
+#pragma unroll
+                            for (int cc = 0; cc < kBN / 64; ++cc) {
+                                if (KIND == KIND_RAGGED_M)
+                                    tma_load_3d(sB + cc * kBK * 128, mB, &ctl->full[stage],
+                                                ti.n0 + cc * 64, red, ti.e);
+                                else
+                                    tma_load_2d(sB + cc * kBK * 128, mB, &ctl->full[stage],
+                                                ti.n0 + cc * 64, red);
+                            }
+                        }
+                    }
+                    ++issued;
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Let every TMA copy this thread issued land before the CTA can exit.
+            const int64_t pend = issued < kStages ? issued : kStages;
+            for (int64_t j = 0; j < pend; ++j) {
+                if (--stage < 0) { stage = kStages - 1; phase ^= 1u; }
+                int dummy = 0;
+                mbar_wait(&ctl->full[stage], phase, reinterpret_cast<volatile int*>(&dummy), p.status);
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------- MMA issuer --
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t acc_count = 0;
+        bool ok = true, any_mma = false;
+        for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            const TileInfo ti = decode_tile<KIND>(t, p, s_off, s_tp);
+            if (ti.nkb == 0) continue;
+            const uint32_t buf = acc_count & 1u;
+            const uint32_t acc_phase = (acc_count >> 1) & 1u;
+            if (!warp_wait(&ctl->tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + buf * kBN;
+            for (int kb = 0; kb < ti.nkb; ++kb) {
+                if (!warp_wait(&ctl->full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sA = stage0 + stage * kStageBytes;
+                const uint32_t sB = sA + kABytes;
+                int ksteps = kBK / 16;
+                if (KIND == KIND_RAGGED_K) {
+                    const int valid = min(kBK, ti.red_len - kb * kBK);
+                    if (valid < kBK) {
+                        ksteps = (valid + 15) / 16;
+                        const int zr_end = ksteps * 16;
+                        // rows [valid, zr_end) of dense (TMA) operands hold the next
+                        // expert's rows: overwrite them with zeros.
+                        const int nz = zr_end - valid;
+                        if (nz > 0) {
+                            const uint4 z = make_uint4(0, 0, 0, 0);
+                            if (!A_GATHER) {
+                                for (int idx = lane; idx < nz * (kBM / 64) * 8; idx += 32) {
+                                    const int piece = idx & 7, rest = idx >> 3;
+                                    const int cc = rest % (kBM / 64), r = valid + rest / (kBM / 64);
+                                    *reinterpret_cast<uint4*>(stage_base + stage * kStageBytes + cc * kBK * 128 + r * 128 + piece * 16) = z;
+                                }
+                            }
+                            if (!B_GATHER) {
+                                for (int idx = lane; idx < nz * (kBN / 64) * 8; idx += 32) {
+                                    const int piece = idx & 7, rest = idx >> 3;
+                                    const int cc = rest % (kBN / 64), r = valid + rest / (kBN / 64);
+                                    *reinterpret_cast<uint4*>(stage_base + stage * kStageBytes + kABytes + cc * kBK * 128 + r * 128 + piece * 16) = z;
+                                }
+                            }
+                            fence_proxy_async_smem();
+                        }
+                        __syncwarp();
+                    }
+                }
+                if (lane == 0) {
+                    for (int ks = 0; ks < ksteps; ++ks) {
+                        umma_bf16(d_tmem, operand_desc<A_MN>(sA, ks), operand_desc<B_MN>(sB, ks),
+                                  Tr::kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&ctl->empty[stage]);
+                    any_mma = true;
+                }
+                __syncwarp();
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            if (lane == 0) umma_commit(&ctl->tmem_full[buf]);
+            __syncwarp();
+            ++acc_count;
+        }
+        // All MMAs of this thread finish before TMEM is released.
+        if (lane == 0 && any_mma) {
+            umma_commit(&ctl->drain);
+            int dummy = 0;
+            mbar_wait(&ctl->drain, 0, reinterpret_cast<volatile int*>(&dummy), p.status);
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ----------------------------------------------------- epilogue --
+        const int q = warp & 3;        // TMEM lane quarter this warp may access
+        const int r = q * 32 + lane;   // tile row of this thread
+        uint32_t acc_count = 0;
+        for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+            const TileInfo ti = decode_tile<KIND>(t, p, s_off, s_tp);
+            const int ncols = tile_cols<KIND>(p, ti.e);
+            // destination row, scale, output base
+            uint16_t* out = p.out;
+            int64_t ld = p.ld_out;
+            int64_t dest = -1;
+            float sc = 1.0f;
+            if (r < ti.rows) {
+                if (KIND == KIND_RAGGED_M) {
+                    const int64_t i = ti.row0 + r;
+                    dest = i;
+                    if (p.scatter_out || p.scale) {
+                        const int32_t f = p.gather_idx[i];
+                        if (f < 0 || f >= p.R) { set_status(p.status, GG_DEV_BAD_ROW_INDEX); dest = -1; }
+                        else {
+                            if (p.scatter_out) dest = f;
+                            if (p.scale) sc = p.scale[f];
+                        }
+                    }
+                } else if (KIND == KIND_RAGGED_K) {
+                    dest = static_cast<int64_t>(ti.e) * p.M + ti.row0 + r;
+                } else {
+                    out = p.dual[ti.e].out;
+                    ld = p.dual[ti.e].ld_out;
+                    dest = ti.row0 + r;
+                }
+            }
+            uint16_t* orow = dest >= 0 ? out + dest * ld : nullptr;
+            if (ti.nkb == 0) {
+                if (orow) {
+                    for (int c = ti.n0; c < min(ti.n0 + kBN, ncols); c += 8)
+                        *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+                }
+                continue;
+            }
+            const uint32_t buf = acc_count & 1u;
+            const uint32_t acc_phase = (acc_count >> 1) & 1u;
+            if (!warp_wait(&ctl->tmem_full[buf], acc_phase, abort_flag, p.status)) break;
+            tc_fence_after();
+            const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN;
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr0 + c * 32, v);
+                tmem_ld_wait();
+                const int col0 = ti.n0 + c * 32;
+                if (orow) {
+#pragma unroll
+                    for (int pc = 0; pc < 4; ++pc) {
+                        const int col = col0 + pc * 8;
+                        if (col < ncols) {
+                            uint4 o;
+                            o.x = pack_bf16x2(__uint_as_float(v[pc * 8 + 0]) * sc, __uint_as_float(v[pc * 8 + 1]) * sc);
+                            o.y = pack_bf16x2(__uint_as_float(v[pc * 8 + 2]) * sc, __uint_as_float(v[pc * 8 + 3]) * sc);
+                            o.z = pack_bf16x2(__uint_as_float(v[pc * 8 + 4]) * sc, __uint_as_float(v[pc * 8 + 5]) * sc);
+                            o.w = pack_bf16x2(__uint_as_float(v[pc * 8 + 6]) * sc, __uint_as_float(v[pc * 8 + 7]) * sc);
+                            *reinterpret_cast<uint4*>(orow + col) = o;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->tmem_empty[buf]);
+            ++acc_count;
+        }
+    } else {
+        // ---------------------------------------------- gather producers --
+        if (Tr::kAnyGather) {
+            const int gt = threadIdx.x - 6 * 32;  // 0 .. 127
+            int stage = 0;
+            uint32_t phase = 0;
+            int pend_stage[kGatherDepth + 1];
+            int npend = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                const TileInfo ti = decode_tile<KIND>(t, p, s_off, s_tp);
+                // K-major gathered A: fixed source rows for the whole tile.
+                const uint16_t* arow[8];
+                if (A_GATHER && !A_MN) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int rr = (gt >> 3) + 16 * j;
+                        arow[j] = nullptr;
+                        if (rr < ti.rows) {
+                            const int64_t src = gather_row(p, p.ga, ti.row0 + rr);
+                            if (src >= 0) arow[j] = p.ga.ptr + src * p.ga.ld;
+                        }
+                    }
+                }
+                for (int kb = 0; kb < ti.nkb; ++kb) {
+                    if (!warp_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    const uint32_t sA = stage0 + stage * kStageBytes;
+                    const uint32_t sB = sA + kABytes;
+                    if (A_GATHER) {
+                        if (!A_MN) {
+                            const int c = gt & 7;
+                            const int64_t col = static_cast<int64_t>(kb) * kBK + c * 8;
+                            const bool cv = col < p.ga.cols;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int rr = (gt >> 3) + 16 * j;
+                                const uint32_t dst = sA + rr * 128 + ((c ^ (rr & 7)) << 4);
+                                const bool v = cv && arow[j] != nullptr;
+                                cp_async_16(dst, v ? static_cast<const void*>(arow[j] + col) : p.ga.ptr, v ? 16u : 0u);
+                            }
+                        } else {
+                            // MN-major: reduction rows are gathered rows; 16 pieces of 8 elements per row.
+                            const int pc = gt & 15;
+                            const int64_t mn = ti.row0 + pc * 8;
+                            const bool mv = mn < p.ga.cols;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int rr = (gt >> 4) + 8 * j;
+                                const int64_t kr = static_cast<int64_t>(kb) * kBK + rr;
+                                const uint16_t* src = nullptr;
+                                if (mv && kr < ti.red_len) {
+                                    const int64_t sr = gather_row(p, p.ga, ti.red0 + kr);
+                                    if (sr >= 0) src = p.ga.ptr + sr * p.ga.ld + mn;
+                                }
+                                const uint32_t dst = sA + (pc >> 3) * (kBK * 128) + rr * 128 + (((pc & 7) ^ (rr & 7)) << 4);
+                                cp_async_16(dst, src ? static_cast<const void*>(src) : p.ga.ptr, src ? 16u : 0u);
+                            }
+                        }
+                    }
+                    if (B_GATHER) {
+                        // Only MN-major gathered B occurs (dW with the forward's token gather).
+                        const int pc = gt & 31;
+                        const int64_t mn = static_cast<int64_t>(ti.n0) + pc * 8;
+                        const bool mv = mn < p.gb.cols;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int rr = (gt >> 5) + 4 * j;
+                            const int64_t kr = static_cast<int64_t>(kb) * kBK + rr;
+                            const uint16_t* src = nullptr;
+                            if (mv && kr < ti.red_len) {
+                                const int64_t sr = gather_row(p, p.gb, ti.red0 + kr);
+                                if (sr >= 0) src = p.gb.ptr + sr * p.gb.ld + mn;
+                            }
+                            const uint32_t dst = sB + (pc >> 3) * (kBK * 128) + rr * 128 + (((pc & 7) ^ (rr & 7)) << 4);
+                            cp_async_16(dst, src ? static_cast<const void*>(src) : p.gb.ptr, src ? 16u : 0u);
+                        }
+                    }
+                    cp_async_commit();
+                    pend_stage[npend++] = stage;
+                    if (npend > kGatherDepth) {
+                        cp_async_wait<kGatherDepth>();
+                        fence_proxy_async_smem();
+                        mbar_arrive(&ctl->full[pend_stage[0]]);
+#pragma unroll
+                        for (int j = 0; j < kGatherDepth; ++j) pend_stage[j] = pend_stage[j + 1];
+                        --npend;
+                    }
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            for (int j = 0; j < npend; ++j) mbar_arrive(&ctl->full[pend_stage[j]]);
+        }
+    }
+
+    // ----------------------------------------------------------- teardown --
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host --
+
+bool encode_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer);
+bool encode_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t stride1_elems, uint64_t stride2_elems, uint32_t b0, uint32_t b1);
+int num_sms();
+void record_cuda_error(cudaError_t e);
+
+template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER>
+int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
+                const CUtensorMap& b1, const GemmParams& p, int64_t tile_bound, cudaStream_t stream) {
+    using Tr = GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER>;
+    auto kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER>;
+    const size_t smem = gemm_smem_bytes(p.E);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(gemm_smem_bytes(GG_MAX_EXPERTS)));
+    if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+    const int64_t sms = num_sms();
+    const int64_t grid = tile_bound < sms ? (tile_bound > 0 ? tile_bound : 1) : sms;
+    kern<<<static_cast<unsigned>(grid), Tr::kThreads, smem, stream>>>(a0, b0, a1, b1, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+    return GG_OK;
+}
+
+}  // namespace gg

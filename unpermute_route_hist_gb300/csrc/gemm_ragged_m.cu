@@ -1,0 +1,121 @@
+// gemm_ragged_m.cu -- entry points whose output rows are ragged per expert:
+// the forward grouped GEMM and the backward dX (interface.py,
+// grouped_gemm_forward and grouped_gemm_dX).  Both run the persistent tcgen05
+// engine of gemm_engine.cuh over the expert-order row tiles.
+#include "gemm_engine.cuh"
+
+namespace gg {
+int combine_launch(const uint16_t* Y, const int32_t* row_id_map, const float* topk_w, int64_t T,
+                   int topk, int64_t N, uint16_t* out, int32_t* status, cudaStream_t stream);
+}
+
+using namespace gg;
+
+namespace {
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Upper bound on the expert-order row tiles (matmul_ogs.py, RoutingData.n_blocks).
+int64_t row_tile_bound(int64_t R, int E) {
+    if (R <= E) return R;
+    return (R - E + 1 + kBM - 1) / kBM + E - 1;
+}
+
+GemmParams base_params(int E, int topk, int64_t R, const int32_t* m_sizes, const int32_t* gather_idx,
+                       int32_t* status) {
+    GemmParams p{};
+    p.E = E;
+    p.topk = topk;
+    p.R = R;
+    p.m_sizes = m_sizes;
+    p.gather_idx = gather_idx;
+    p.status = status;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gg_forward(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
+               const int32_t* gather_idx, const float* topk_w, int64_t T, int topk, int E,
+               int64_t N, int64_t K, int permute_x, int permute_y, int fuse_mul_post, gg_bf16* Y,
+               int32_t* status, void* stream) {
+    if (T < 0 || topk < 1 || E < 1 || N < 0 || K < 0) return GG_ERR_INVALID_ARG;
+    if (topk > GG_MAX_TOPK || E > GG_MAX_EXPERTS || N % 8 || K % 8) return GG_ERR_UNSUPPORTED;
+    const int64_t R = T * topk;
+    if (R >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+        return GG_ERR_UNSUPPORTED;
+    if ((permute_x || permute_y) && !gather_idx) return GG_ERR_INVALID_ARG;
+    if (fuse_mul_post && (!permute_y || !topk_w)) return GG_ERR_INVALID_ARG;
+    if (R == 0 || N == 0) return GG_OK;
+    if (!X || !W || !m_sizes || !Y) return GG_ERR_INVALID_ARG;
+    if (!al16(X) || !al16(W) || !al16(Y)) return GG_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        const cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(R * N) * 2, st);
+        if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+        return GG_OK;
+    }
+    GemmParams p = base_params(E, topk, R, m_sizes, gather_idx, status);
+    p.N = static_cast<int>(N);
+    p.Kred = static_cast<int>(K);
+    p.out = Y;
+    p.ld_out = N;
+    p.scatter_out = permute_y ? 1 : 0;
+    p.scale = fuse_mul_post ? topk_w : nullptr;
+    CUtensorMap mA{}, mB{};
+    if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN)) return GG_ERR_CUDA;
+    const int64_t bound = row_tile_bound(R, E) * ((N + kBN - 1) / kBN);
+    if (permute_x) {
+        p.ga = GatherSrc{X, K, T, K, ROW_TOKEN};
+        mA = mB;  // unused
+        return launch_gemm<KIND_RAGGED_M, false, false, true, false>(mA, mB, mA, mB, p, bound, st);
+    }
+    if (!encode_map_2d(&mA, X, K, R, K, kBK, kBM)) return GG_ERR_CUDA;
+    return launch_gemm<KIND_RAGGED_M, false, false, false, false>(mA, mB, mA, mB, p, bound, st);
+}
+
+int gg_backward_dX(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes,
+                   const int32_t* gather_idx, int64_t T, int topk, int E, int64_t N, int64_t K,
+                   int permute_x, int permute_y, gg_bf16* dX, gg_bf16* dX_tok, int32_t* status,
+                   void* stream) {
+    if (T < 0 || topk < 1 || E < 1 || N < 0 || K < 0) return GG_ERR_INVALID_ARG;
+    if (topk > GG_MAX_TOPK || E > GG_MAX_EXPERTS || N % 8 || K % 8) return GG_ERR_UNSUPPORTED;
+    const int64_t R = T * topk;
+    if (R >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+        return GG_ERR_UNSUPPORTED;
+    if ((permute_x || permute_y) && !gather_idx) return GG_ERR_INVALID_ARG;
+    if (dX_tok && !permute_x) return GG_ERR_INVALID_ARG;
+    if (R == 0 || K == 0) return GG_OK;
+    if (!dY || !W || !m_sizes || !dX) return GG_ERR_INVALID_ARG;
+    if (!al16(dY) || !al16(W) || !al16(dX) || (dX_tok && !al16(dX_tok))) return GG_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int rc = GG_OK;
+    if (N == 0) {
+        const cudaError_t e = cudaMemsetAsync(dX, 0, static_cast<size_t>(R * K) * 2, st);
+        if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+    } else {
+        GemmParams p = base_params(E, topk, R, m_sizes, gather_idx, status);
+        p.N = static_cast<int>(K);      // output columns
+        p.Kred = static_cast<int>(N);   // reduction over the forward's N
+        p.out = dX;
+        p.ld_out = K;
+        p.scatter_out = permute_x ? 1 : 0;
+        CUtensorMap mA{}, mB{};
+        // B[k, n] = W[e][n, k]: MN-major, 64-wide k chunks over 64 rows of n.
+        if (!encode_map_3d(&mB, W, K, N, E, K, N * K, 64, kBK)) return GG_ERR_CUDA;
+        const int64_t bound = row_tile_bound(R, E) * ((K + kBN - 1) / kBN);
+        if (permute_y) {
+            p.ga = GatherSrc{dY, N, R, N, ROW_SLOT};
+            rc = launch_gemm<KIND_RAGGED_M, false, true, true, false>(mB, mB, mB, mB, p, bound, st);
+        } else {
+            if (!encode_map_2d(&mA, dY, N, R, N, kBK, kBM)) return GG_ERR_CUDA;
+            rc = launch_gemm<KIND_RAGGED_M, false, true, false, false>(mA, mB, mA, mB, p, bound, st);
+        }
+    }
+    if (rc != GG_OK || !dX_tok) return rc;
+    return combine_launch(dX, nullptr, nullptr, T, topk, K, dX_tok, status, st);
+}
+
+}  // extern "C"

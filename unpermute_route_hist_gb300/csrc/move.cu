@@ -1,0 +1,128 @@
+// move.cu -- the two HBM-bound row movers of the MoE path.
+//
+//  permute            token rows into expert order (wall_x backend.py, permute;
+//                     interface.py, permute_x).  Token-stationary: each token
+//                     row X[t] is read from HBM once and written to the topk
+//                     rows row_id_map[t*topk + j] of Xp.
+//  unpermute_combine  expert outputs back to token order with the weighted sum
+//                     over a token's slots (backend.py, unpermute; matmul_ogs.py,
+//                     matmul_ogs_torch's fp32 accumulation).  Output-stationary
+//                     and deterministic: out[t] sums its slots in slot order.
+//
+// Both move whole rows as 16-byte vectors (row widths are multiples of 8
+// bf16), one CTA per row in a grid that is a multiple of the SM count.
+#include "common.cuh"
+
+namespace gg {
+namespace {
+
+constexpr int kMoveThreads = 256;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__global__ void __launch_bounds__(kMoveThreads)
+permute_kernel(const uint4* __restrict__ X, const int32_t* __restrict__ row_id_map, int64_t T,
+               int topk, int64_t row_vecs, uint4* __restrict__ Xp, int64_t R, int32_t* status) {
+    __shared__ int32_t dst_s[GG_MAX_TOPK];
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x < topk) {
+            int32_t d = row_id_map[t * topk + threadIdx.x];
+            if (d < 0 || d >= R) {
+                set_status(status, GG_DEV_BAD_ROW_INDEX);
+                d = -1;
+            }
+            dst_s[threadIdx.x] = d;
+        }
+        __syncthreads();
+        const uint4* src = X + t * row_vecs;
+        for (int64_t c = threadIdx.x; c < row_vecs; c += kMoveThreads) {
+            const uint4 v = ld_stream(src + c);
+            for (int j = 0; j < topk; ++j) {
+                const int32_t d = dst_s[j];
+                if (d >= 0) Xp[static_cast<int64_t>(d) * row_vecs + c] = v;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void bf16x8_fma(float (&acc)[8], const uint4& v, float w) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]);
+        acc[2 * q] = fmaf(w, f.x, acc[2 * q]);
+        acc[2 * q + 1] = fmaf(w, f.y, acc[2 * q + 1]);
+    }
+}
+
+__global__ void __launch_bounds__(kMoveThreads)
+combine_kernel(const uint4* __restrict__ Y, const int32_t* __restrict__ row_id_map,
+               const float* __restrict__ topk_w, int64_t T, int topk, int64_t row_vecs, int64_t R,
+               uint4* __restrict__ out, int32_t* status) {
+    __shared__ int32_t src_s[GG_MAX_TOPK];
+    __shared__ float w_s[GG_MAX_TOPK];
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x < topk) {
+            const int64_t f = t * topk + threadIdx.x;
+            int32_t s = row_id_map ? row_id_map[f] : static_cast<int32_t>(f);
+            if (s < 0 || s >= R) {
+                set_status(status, GG_DEV_BAD_ROW_INDEX);
+                s = -1;
+            }
+            src_s[threadIdx.x] = s;
+            w_s[threadIdx.x] = topk_w ? topk_w[f] : 1.0f;
+        }
+        __syncthreads();
+        for (int64_t c = threadIdx.x; c < row_vecs; c += kMoveThreads) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < topk; ++j) {
+                const int32_t s = src_s[j];
+                if (s >= 0) bf16x8_fma(acc, ld_stream(Y + static_cast<int64_t>(s) * row_vecs + c), w_s[j]);
+            }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            out[t * row_vecs + c] = o;
+        }
+    }
+}
+
+unsigned move_grid(int64_t rows) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t g = static_cast<int64_t>(sms) * 8;  // 8 resident 256-thread CTAs per SM
+    return static_cast<unsigned>(rows < g ? rows : g);
+}
+
+}  // namespace
+
+int permute_launch(const uint16_t* X, const int32_t* row_id_map, int64_t T, int topk, int64_t K,
+                   uint16_t* Xp, int32_t* status, cudaStream_t stream) {
+    const int64_t R = T * topk;
+    permute_kernel<<<move_grid(T), kMoveThreads, 0, stream>>>(
+        reinterpret_cast<const uint4*>(X), row_id_map, T, topk, K / 8, reinterpret_cast<uint4*>(Xp),
+        R, status);
+    return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
+}
+
+int combine_launch(const uint16_t* Y, const int32_t* row_id_map, const float* topk_w, int64_t T,
+                   int topk, int64_t N, uint16_t* out, int32_t* status, cudaStream_t stream) {
+    const int64_t R = T * topk;
+    combine_kernel<<<move_grid(T), kMoveThreads, 0, stream>>>(
+        reinterpret_cast<const uint4*>(Y), row_id_map, topk_w, T, topk, N / 8, R,
+        reinterpret_cast<uint4*>(out), status);
+    return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
+}
+
+}  // namespace gg
