@@ -60,6 +60,7 @@ typedef uint16_t gg_bf16;
 
 #define GG_MAX_EXPERTS 2048
 #define GG_MAX_TOPK 64
+#define GG_ROUTE_NOALLOC_SCRATCH_BYTES (1u << 20)
 
 /* Human-readable text for a GG_* return code (static storage). */
 const char* gg_status_string(int code);
@@ -93,6 +94,27 @@ int gg_route_hist_offsets(const int32_t* topk_ids, int64_t T, int topk, int E, i
                           int32_t* m_sizes, int32_t* offsets, int32_t* padded_offsets,
                           int32_t* gather_idx, int32_t* row_id_map, void* workspace,
                           size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ------------------------------------------------ route, allocation-free --
+ * No counterpart on the pages.  Same outputs as gg_route_hist_offsets, for
+ * callers that cannot allocate device memory or pass a workspace: a runtime
+ * that owns all device memory in its own arena and hands this code only its
+ * input and output buffers, or a latency-critical path that must not pay for
+ * an allocation.  There is no workspace argument: the counting sort's scratch
+ * is a static device array of GG_ROUTE_NOALLOC_SCRATCH_BYTES (1 MiB) that
+ * every GPU loading the library holds until the process exits.
+ *  - The first call on each device looks up that array's device address
+ *    (once per device, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the array: calls that overlap on the GPU race on it, so
+ *    the caller must serialise them.  No state carries over between calls.
+ *  - A problem whose scratch, ceil(T*topk/256) * E * 4 bytes, exceeds the
+ *    array returns GG_ERR_WORKSPACE without launching.
+ * Allocates nothing. */
+int gg_route_hist_offsets_noalloc(const int32_t* topk_ids, int64_t T, int topk, int E,
+                                  int pad_block, int32_t* m_sizes, int32_t* offsets,
+                                  int32_t* padded_offsets, int32_t* gather_idx,
+                                  int32_t* row_id_map, int32_t* status, void* stream);
 
 /* ---------------------------------------------------------------- permute --
  * Token rows into expert order ([W] permute; [U] permute_x): for every slot f

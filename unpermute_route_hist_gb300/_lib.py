@@ -26,6 +26,8 @@ SIGNATURES = {
     "gg_route_workspace_size": (_sz, [_i64, _int, _int]),
     "gg_route_hist_offsets": (_int, [_vp, _i64, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                      _vp, _vp]),
+    "gg_route_hist_offsets_noalloc": (_int, [_vp, _i64, _int, _int, _int, _vp, _vp, _vp, _vp, _vp,
+                                             _vp, _vp]),
     "gg_permute": (_int, [_vp, _vp, _i64, _int, _i64, _vp, _vp, _vp]),
     "gg_unpermute_combine": (_int, [_vp, _vp, _vp, _i64, _int, _i64, _vp, _vp, _vp]),
     "gg_forward": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _int, _int,
@@ -50,6 +52,7 @@ GG_DEV_SIZES_MISMATCH = 3
 GG_DEV_TIMEOUT = 4
 GG_MAX_EXPERTS = 2048
 GG_MAX_TOPK = 64
+GG_ROUTE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 _lock = threading.Lock()
 _lib = None
