@@ -437,7 +437,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gg", choices=["gg", "reference"])
     ap.add_argument("--config", default="mlp8")
-    ap.add_argument("--ref-rows", type=int, default=16)
+    ap.add_argument("--ref-rows", type=int, default=96)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     from unpermute_route_hist_gb300 import synth

@@ -15,7 +15,8 @@
 //   warp 0      tile scheduler + TMA producer (lane 0) for dense operands
 //   warp 1      TMEM allocation + MMA issue (lane 0); zeroes ragged tails
 //   warps 2-5   epilogue: TMEM -> registers -> scale -> bf16 -> global rows
-//   warps 6-9   (only with a gathered operand) cp.async row-gather producers
+//   warps 6-9   (only with a gathered operand) cp.async row-gather producers;
+//               each thread's copies arrive on the stage barrier as they land
 // Every role walks the same static tile list (tile = blockIdx.x + j*gridDim.x),
 // decoded from m_sizes in shared memory, so no role sends tile ids to another.
 //
@@ -40,7 +41,6 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators
 constexpr int kGroupM = 16;             // m-tiles per raster group (L2 reuse)
 constexpr int kGatherWarps = 4;
-constexpr int kGatherDepth = 2;         // cp.async stages in flight per thread
 
 enum GemmKind { KIND_RAGGED_M = 0, KIND_RAGGED_K = 1, KIND_DUAL = 2 };
 // Row index of a gathered operand row for expert-order row i.
@@ -422,6 +422,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     }
                 }
                 if (lane == 0) {
+                    // cp.async writes are generic-proxy; order them before the
+                    // tensor core's async-proxy reads of this stage
+                    if (Tr::kAnyGather) fence_proxy_async_smem();
                     for (int ks = 0; ks < ksteps; ++ks) {
                         umma_bf16(d_tmem, operand_desc<A_MN>(sA, ks), operand_desc<B_MN>(sB, ks),
                                   Tr::kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
@@ -518,32 +521,75 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         }
     } else {
         // ---------------------------------------------- gather producers --
+        // Index loads run one step ahead of the copies that need them: the slot
+        // numbers for the next stage (MN-major, dW) or the next tile (K-major)
+        // are loaded while the current copies are issued, so no cp.async waits
+        // on a dependent index load.
         if (Tr::kAnyGather) {
             const int gt = threadIdx.x - 6 * 32;  // 0 .. 127
             int stage = 0;
             uint32_t phase = 0;
-            int pend_stage[kGatherDepth + 1];
-            int npend = 0;
             bool ok = true;
+            // K-major gathered A: the tile's 8 rows of this thread (fixed over the tile).
+            int32_t a_next[8];
+            auto fetch_a_rows = [&](int64_t tt) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) a_next[j] = -1;
+                if (tt < total_tiles) {
+                    const TileInfo tn = decode_tile<KIND>(tt, p, s_off, s_tp);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int rr = (gt >> 3) + 16 * j;
+                        if (rr < tn.rows) a_next[j] = p.gather_idx[tn.row0 + rr];
+                    }
+                }
+            };
+            // MN-major gathered rows of the next stage (A: 8 rows, B: 16 rows per thread).
+            int32_t ra_next[8], rb_next[16];
+            auto fetch_red_rows = [&](const TileInfo& tn, int kb) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int64_t kr = static_cast<int64_t>(kb) * kBK + (gt >> 4) + 8 * j;
+                    ra_next[j] = (A_GATHER && A_MN && kb < tn.nkb && kr < tn.red_len) ? p.gather_idx[tn.red0 + kr] : -1;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int64_t kr = static_cast<int64_t>(kb) * kBK + (gt >> 5) + 4 * j;
+                    rb_next[j] = (B_GATHER && kb < tn.nkb && kr < tn.red_len) ? p.gather_idx[tn.red0 + kr] : -1;
+                }
+            };
+            // slot number -> source row of a gathered operand, -1 if absent or out of range
+            auto src_row = [&](const GatherSrc& g, int32_t f) -> int64_t {
+                if (f < 0) return -1;
+                const int64_t r = g.row_mode == ROW_TOKEN ? static_cast<int64_t>(f) / p.topk : static_cast<int64_t>(f);
+                if (r >= g.rows) { set_status(p.status, GG_DEV_BAD_ROW_INDEX); return -1; }
+                return r;
+            };
+            if (A_GATHER && !A_MN) fetch_a_rows(blockIdx.x);
             for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
                 const TileInfo ti = decode_tile<KIND>(t, p, s_off, s_tp);
-                // K-major gathered A: fixed source rows for the whole tile.
                 const uint16_t* arow[8];
                 if (A_GATHER && !A_MN) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const int rr = (gt >> 3) + 16 * j;
-                        arow[j] = nullptr;
-                        if (rr < ti.rows) {
-                            const int64_t src = gather_row(p, p.ga, ti.row0 + rr);
-                            if (src >= 0) arow[j] = p.ga.ptr + src * p.ga.ld;
-                        }
+                        const int64_t sr = src_row(p.ga, a_next[j]);
+                        arow[j] = sr >= 0 ? p.ga.ptr + sr * p.ga.ld : nullptr;
                     }
+                    fetch_a_rows(t + gridDim.x);
                 }
+                if (A_MN || B_GATHER) fetch_red_rows(ti, 0);
                 for (int kb = 0; kb < ti.nkb; ++kb) {
                     if (!warp_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     const uint32_t sA = stage0 + stage * kStageBytes;
                     const uint32_t sB = sA + kABytes;
+                    int32_t ra[8], rb[16];
+                    if (A_MN || B_GATHER) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) ra[j] = ra_next[j];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) rb[j] = rb_next[j];
+                        fetch_red_rows(ti, kb + 1);
+                    }
                     if (A_GATHER) {
                         if (!A_MN) {
                             const int c = gt & 7;
@@ -564,14 +610,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
                                 const int rr = (gt >> 4) + 8 * j;
-                                const int64_t kr = static_cast<int64_t>(kb) * kBK + rr;
-                                const uint16_t* src = nullptr;
-                                if (mv && kr < ti.red_len) {
-                                    const int64_t sr = gather_row(p, p.ga, ti.red0 + kr);
-                                    if (sr >= 0) src = p.ga.ptr + sr * p.ga.ld + mn;
-                                }
+                                const int64_t sr = mv ? src_row(p.ga, ra[j]) : -1;
                                 const uint32_t dst = sA + (pc >> 3) * (kBK * 128) + rr * 128 + (((pc & 7) ^ (rr & 7)) << 4);
-                                cp_async_16(dst, src ? static_cast<const void*>(src) : p.ga.ptr, src ? 16u : 0u);
+                                cp_async_16(dst, sr >= 0 ? static_cast<const void*>(p.ga.ptr + sr * p.ga.ld + mn) : p.ga.ptr,
+                                            sr >= 0 ? 16u : 0u);
                             }
                         }
                     }
@@ -583,32 +625,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int rr = (gt >> 5) + 4 * j;
-                            const int64_t kr = static_cast<int64_t>(kb) * kBK + rr;
-                            const uint16_t* src = nullptr;
-                            if (mv && kr < ti.red_len) {
-                                const int64_t sr = gather_row(p, p.gb, ti.red0 + kr);
-                                if (sr >= 0) src = p.gb.ptr + sr * p.gb.ld + mn;
-                            }
+                            const int64_t sr = mv ? src_row(p.gb, rb[j]) : -1;
                             const uint32_t dst = sB + (pc >> 3) * (kBK * 128) + rr * 128 + (((pc & 7) ^ (rr & 7)) << 4);
-                            cp_async_16(dst, src ? static_cast<const void*>(src) : p.gb.ptr, src ? 16u : 0u);
+                            cp_async_16(dst, sr >= 0 ? static_cast<const void*>(p.gb.ptr + sr * p.gb.ld + mn) : p.gb.ptr,
+                                        sr >= 0 ? 16u : 0u);
                         }
                     }
-                    cp_async_commit();
-                    pend_stage[npend++] = stage;
-                    if (npend > kGatherDepth) {
-                        cp_async_wait<kGatherDepth>();
-                        fence_proxy_async_smem();
-                        mbar_arrive(&ctl->full[pend_stage[0]]);
-#pragma unroll
-                        for (int j = 0; j < kGatherDepth; ++j) pend_stage[j] = pend_stage[j + 1];
-                        --npend;
-                    }
+                    // the stage's barrier gets this thread's arrival when its copies land
+                    cp_async_mbar_arrive(&ctl->full[stage]);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
             }
+            // every copy lands before the CTA can exit
             cp_async_wait<0>();
-            fence_proxy_async_smem();
-            for (int j = 0; j < npend; ++j) mbar_arrive(&ctl->full[pend_stage[j]]);
         }
     }
 
