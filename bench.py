@@ -4,12 +4,17 @@ A step is one pass of the whole hot path over one batch of synthetic input
 (configuration "mlp8": T=8192 tokens, hidden 4096, expert intermediate 14336
 (gate_up N = 28672), E=8 experts, top-2):
     route          gg_route_hist_offsets   histogram, offsets, stable permutation
-    permute        gg_permute              X -> expert order (input of dW1)
-    GEMM1 fwd      gg_forward              permute_x (token gather fused)
+    permute        gg_permute              X -> expert order (Xp)
+    GEMM1 fwd      gg_forward              Xp (dense TMA operands)
     GEMM2 fwd      gg_forward              permute_y (scatter to token order fused)
     combine        gg_unpermute_combine    weighted top-k combine -> [T, hidden]
-    GEMM2 bwd      gg_backward_dX (permute_y), gg_backward_dW (permute_y)
-    GEMM1 bwd      gg_backward_dX (permute_x, + top-k token sum), gg_backward_dW
+    permute        gg_permute              dY2 (token-slot order) -> expert order
+    GEMM2 bwd      gg_backward_dX, gg_backward_dW on the expert-ordered dY2
+    GEMM1 bwd      gg_backward_dX (permute_x scatter store + top-k token sum),
+                   gg_backward_dW on Xp
+Materialising the expert-ordered operands once (about 0.03-0.05 ms each) lets
+every GEMM read dense TMA tiles; the fused-gather variants of the same calls
+compute the same values (tests) and are timed separately under "variants".
 The GEMM2 input stands in for act(GEMM1) (a seeded tensor), and the output
 gradients are seeded tensors; FLOPs counted are 2*R*N*K per GEMM pass (6
 passes), padding rows not counted.
@@ -269,7 +274,9 @@ def run_gg(args, cfg):
     passes = _gemm_passes(cfg)
     step_flops = sum(passes.values())
 
-    ev_names = ["route", "permute", "fwd1", "fwd2", "combine", "dX2", "dW2", "dX1", "dW1"]
+    ev_names = ["route", "permute", "fwd1", "fwd2", "combine", "permute_dY", "dX2", "dW2", "dX1",
+                "dW1"]
+    dYp = torch.empty(R, K, dtype=bf, device=dev)
 
     def step(src, evs=None):
         def mark(i):
@@ -280,7 +287,7 @@ def run_gg(args, cfg):
         mark(1)
         gg.permute(src["X"], r["row_id_map"], k, out=Xp, status=status)
         mark(2)
-        gg.forward(src["X"], W1, r["m_sizes"], r["gather_idx"], None, k, True, False, False, out=H,
+        gg.forward(Xp, W1, r["m_sizes"], r["gather_idx"], None, k, False, False, False, out=H,
                    status=status)
         mark(3)
         gg.forward(src["A2"], W2, r["m_sizes"], r["gather_idx"], None, k, False, True, False, out=Y2,
@@ -288,20 +295,24 @@ def run_gg(args, cfg):
         mark(4)
         gg.unpermute_combine(Y2, None, src["w"], T, k, out=out, status=status)
         mark(5)
-        gg.backward_dX(src["dY2"], W2, r["m_sizes"], r["gather_idx"], T, k, False, True, out=dA2,
-                       status=status)
+        # dY2 arrives in token-slot order (the forward scattered with permute_y)
+        gg.permute(src["dY2"], r["row_id_map"], 1, out=dYp, status=status)
         mark(6)
-        gg.backward_dW(src["A2"], src["dY2"], r["m_sizes"], r["gather_idx"], T, k, False, True,
-                       out=dW2, status=status)
+        gg.backward_dX(dYp, W2, r["m_sizes"], r["gather_idx"], T, k, False, False, out=dA2,
+                       status=status)
         mark(7)
+        gg.backward_dW(src["A2"], dYp, r["m_sizes"], r["gather_idx"], T, k, False, False,
+                       out=dW2, status=status)
+        mark(8)
         gg.backward_dX(src["dH"], W1, r["m_sizes"], r["gather_idx"], T, k, True, False,
                        token_sum=True, out=dX1, out_tok=dXt, status=status)
-        mark(8)
+        mark(9)
         gg.backward_dW(Xp, src["dH"], r["m_sizes"], r["gather_idx"], T, k, False, False, out=dW1,
                        status=status)
-        mark(9)
+        mark(10)
 
-    launches_per_step = 4 + 1 + 1 + 1 + 1 + 1 + 1 + 2 + 1  # route(4) permute fwd fwd combine dX dW dX(+sum) dW
+    # route(4) permute fwd fwd combine permute dX dW dX(+token sum) dW
+    launches_per_step = 4 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 2 + 1
     src = dict(d, ids=ids, w=wts)
     for _ in range(max(args.warmup, 3)):
         step(src)
@@ -378,10 +389,39 @@ def run_gg(args, cfg):
         e_ms = float(tt.item())
     e_value = step_flops * ws / (e_ms * 1e-3) / 1e12
 
+    # ---- the same passes with the gather fused into the GEMM (outside the step) -
+    def time_call(fn, reps=3):
+        fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    rr = o
+    variants = {
+        "fwd1_fused_token_gather": (time_call(lambda: gg.forward(
+            src["X"], W1, rr["m_sizes"], rr["gather_idx"], None, k, True, False, False, out=H,
+            status=status)), passes["fwd1"]),
+        "dX2_fused_slot_gather": (time_call(lambda: gg.backward_dX(
+            src["dY2"], W2, rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dA2,
+            status=status)), passes["dX2"]),
+        "dW2_fused_slot_gather": (time_call(lambda: gg.backward_dW(
+            src["A2"], src["dY2"], rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dW2,
+            status=status)), passes["dW2"]),
+        "dW1_fused_token_gather": (time_call(lambda: gg.backward_dW(
+            src["X"], src["dH"], rr["m_sizes"], rr["gather_idx"], T, k, True, False, out=dW1,
+            status=status), reps=1), passes["dW1"]),
+    }
+    variants = {n: {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12} for n, (ms, fl) in variants.items()}
+
     # ---- HBM-bound movers: GB/s of the timed permute and combine --------------
     perm_bytes = T * K * 2 + R * K * 2 + R * 4
     comb_bytes = R * K * 2 + R * 4 + T * K * 2  # weights R*4 also read
     comb_bytes += R * 4
+    permdy_bytes = 2 * R * K * 2 + R * 4
 
     if int(status.item()) != 0:
         raise RuntimeError("device status %d after the timed region" % int(status.item()))
@@ -398,7 +438,7 @@ def run_gg(args, cfg):
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": _config_dict(cfg, ws),
-            "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (GEMM1 forward, token gather)",
+            "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (GEMM1 forward, dense TMA operands)",
                          "achieved": achieved, "peak": tflops_sus, "unit": "TFLOP/s",
                          "frac": achieved / tflops_sus, "peak_source": src_kind + " bf16 sustained",
                          "traffic": None},
@@ -406,11 +446,13 @@ def run_gg(args, cfg):
                      "frac_of_peak": sum(passes.values()) / (gemm_ms * 1e-3) / 1e12 / tflops_sus,
                      "ms": {n: per[n] for n in passes}},
             "hbm_movers": {"permute_GBps": perm_bytes / (per["permute"] * 1e-3) / 1e9,
+                           "permute_dY_GBps": permdy_bytes / (per["permute_dY"] * 1e-3) / 1e9,
                            "combine_GBps": comb_bytes / (per["combine"] * 1e-3) / 1e9,
                            "peak_GBps": hbm, "peak_source": src_kind,
                            "permute_frac": perm_bytes / (per["permute"] * 1e-3) / 1e9 / hbm,
                            "combine_frac": comb_bytes / (per["combine"] * 1e-3) / 1e9 / hbm,
                            "route_ms": per["route"]},
+            "variants": variants,
             "e2e": {"value": e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms},
             "gpu_launches": launches_per_step * args.steps,

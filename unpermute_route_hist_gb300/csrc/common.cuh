@@ -70,12 +70,16 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // Wait for the phase with the given parity to complete.  Gives up when the
 // CTA-wide abort flag is raised or after kWaitLimitNs, raising the flag and
 // the device status; returns false then.
+// sleep_ns > 0 backs off between polls: for waits that normally last a long
+// time (an epilogue waiting for a whole tile), so the polling warp leaves its
+// issue slots to the warps doing the work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status) {
+                                          int32_t* status, uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     uint32_t n = 0;
     while (true) {
+        if (sleep_ns) __nanosleep(sleep_ns);
         if (mbar_try_wait(bar, parity)) return true;
         if ((++n & 31u) == 0) {
             if (*abort_flag) return false;
@@ -92,9 +96,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // warp never diverges on the abort path (tcgen05 .sync.aligned operations
 // need the whole warp).  All 32 lanes must call it together.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status) {
+                                          int32_t* status, uint32_t sleep_ns = 0) {
     int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status, sleep_ns) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
     return ok != 0;

@@ -134,7 +134,15 @@ __device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
         const int64_t per_e = static_cast<int64_t>(mt_per) * nt_per;
         const int e = static_cast<int>(t / per_e);
         const int loc = static_cast<int>(t - e * per_e);
-        const int mt = loc % mt_per, nt = loc / mt_per;
+        // grouped raster inside the expert: kGroupM m-tiles x every n-tile, m
+        // fastest, so concurrent CTAs share both A and B tiles in L2 and no
+        // single tile is read by every SM at once
+        const int per_group = kGroupM * nt_per;
+        const int group = loc / per_group;
+        const int first = group * kGroupM;
+        const int gsize = min(mt_per - first, kGroupM);
+        const int gl = loc - group * per_group;
+        const int mt = first + gl % gsize, nt = gl / gsize;
         ti.e = e;
         ti.row0 = static_cast<int64_t>(mt) * kBM;
         ti.rows = min(kBM, p.M - mt * kBM);
@@ -490,7 +498,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             }
             const uint32_t buf = acc_count & 1u;
             const uint32_t acc_phase = (acc_count >> 1) & 1u;
-            if (!warp_wait(&ctl->tmem_full[buf], acc_phase, abort_flag, p.status)) break;
+            if (!warp_wait(&ctl->tmem_full[buf], acc_phase, abort_flag, p.status, 64)) break;
             tc_fence_after();
             const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN;
 #pragma unroll 1
@@ -544,24 +552,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     }
                 }
             };
-            // MN-major gathered rows of the next stage (A: 8 rows, B: 16 rows per thread).
-            int32_t ra_next[8], rb_next[16];
-            auto fetch_red_rows = [&](const TileInfo& tn, int kb) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int64_t kr = static_cast<int64_t>(kb) * kBK + (gt >> 4) + 8 * j;
-                    ra_next[j] = (A_GATHER && A_MN && kb < tn.nkb && kr < tn.red_len) ? p.gather_idx[tn.red0 + kr] : -1;
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int64_t kr = static_cast<int64_t>(kb) * kBK + (gt >> 5) + 4 * j;
-                    rb_next[j] = (B_GATHER && kb < tn.nkb && kr < tn.red_len) ? p.gather_idx[tn.red0 + kr] : -1;
-                }
+            // MN-major gathered operands (dW): the 64 slot numbers of a stage are
+            // loaded cooperatively (lane L holds rows 2L and 2L+1) three stages
+            // before use, then handed to the threads that copy each row by shuffle.
+            const int glane = gt & 31, gw = gt >> 5;
+            int32_t q_lo[4], q_hi[4];  // look-ahead ring, fully unrolled rotation below
+            auto load_stage_idx = [&](const TileInfo& tn, int kb, int32_t& lo, int32_t& hi) {
+                const int64_t k0 = static_cast<int64_t>(kb) * kBK + 2 * glane;
+                lo = (kb < tn.nkb && k0 < tn.red_len) ? p.gather_idx[tn.red0 + k0] : -1;
+                hi = (kb < tn.nkb && k0 + 1 < tn.red_len) ? p.gather_idx[tn.red0 + k0 + 1] : -1;
             };
             // slot number -> source row of a gathered operand, -1 if absent or out of range
             auto src_row = [&](const GatherSrc& g, int32_t f) -> int64_t {
                 if (f < 0) return -1;
-                const int64_t r = g.row_mode == ROW_TOKEN ? static_cast<int64_t>(f) / p.topk : static_cast<int64_t>(f);
+                // 32-bit division: slot numbers are below 2^31
+                const int64_t r = g.row_mode == ROW_TOKEN ? static_cast<int64_t>(static_cast<uint32_t>(f) / static_cast<uint32_t>(p.topk))
+                                                          : static_cast<int64_t>(f);
                 if (r >= g.rows) { set_status(p.status, GG_DEV_BAD_ROW_INDEX); return -1; }
                 return r;
             };
@@ -577,18 +583,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     }
                     fetch_a_rows(t + gridDim.x);
                 }
-                if (A_MN || B_GATHER) fetch_red_rows(ti, 0);
+                constexpr bool kRedGather = (A_GATHER && A_MN) || B_GATHER;
+                if (kRedGather) {
+                    load_stage_idx(ti, 0, q_lo[0], q_hi[0]);
+                    load_stage_idx(ti, 1, q_lo[1], q_hi[1]);
+                    load_stage_idx(ti, 2, q_lo[2], q_hi[2]);
+                }
                 for (int kb = 0; kb < ti.nkb; ++kb) {
-                    if (!warp_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    if (!warp_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, p.status, 32)) { ok = false; break; }
                     const uint32_t sA = stage0 + stage * kStageBytes;
                     const uint32_t sB = sA + kABytes;
-                    int32_t ra[8], rb[16];
-                    if (A_MN || B_GATHER) {
+                    int32_t cur_lo = 0, cur_hi = 0;
+                    if (kRedGather) {
+                        load_stage_idx(ti, kb + 3, q_lo[3], q_hi[3]);
+                        cur_lo = q_lo[0];
+                        cur_hi = q_hi[0];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) ra[j] = ra_next[j];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) rb[j] = rb_next[j];
-                        fetch_red_rows(ti, kb + 1);
+                        for (int j = 0; j < 3; ++j) { q_lo[j] = q_lo[j + 1]; q_hi[j] = q_hi[j + 1]; }
                     }
                     if (A_GATHER) {
                         if (!A_MN) {
@@ -604,13 +615,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                             }
                         } else {
                             // MN-major: reduction rows are gathered rows; 16 pieces of 8 elements per row.
+                            // Row rr = 2*gw + (glane >> 4) + 8j sits in lane rr >> 1 = gw + 4j.
                             const int pc = gt & 15;
                             const int64_t mn = ti.row0 + pc * 8;
                             const bool mv = mn < p.ga.cols;
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
                                 const int rr = (gt >> 4) + 8 * j;
-                                const int64_t sr = mv ? src_row(p.ga, ra[j]) : -1;
+                                const int32_t lo = __shfl_sync(0xffffffffu, cur_lo, gw + 4 * j);
+                                const int32_t hi = __shfl_sync(0xffffffffu, cur_hi, gw + 4 * j);
+                                const int64_t sr = mv ? src_row(p.ga, (glane >> 4) ? hi : lo) : -1;
                                 const uint32_t dst = sA + (pc >> 3) * (kBK * 128) + rr * 128 + (((pc & 7) ^ (rr & 7)) << 4);
                                 cp_async_16(dst, sr >= 0 ? static_cast<const void*>(p.ga.ptr + sr * p.ga.ld + mn) : p.ga.ptr,
                                             sr >= 0 ? 16u : 0u);
@@ -622,10 +636,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         const int pc = gt & 31;
                         const int64_t mn = static_cast<int64_t>(ti.n0) + pc * 8;
                         const bool mv = mn < p.gb.cols;
+                        // Row rr = gw + 4j sits in lane rr >> 1, in its low or high slot by gw & 1.
+                        const int32_t sel = (gw & 1) ? cur_hi : cur_lo;
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int rr = (gt >> 5) + 4 * j;
-                            const int64_t sr = mv ? src_row(p.gb, rb[j]) : -1;
+                            const int32_t f = __shfl_sync(0xffffffffu, sel, (gw + 4 * j) >> 1);
+                            const int64_t sr = mv ? src_row(p.gb, f) : -1;
                             const uint32_t dst = sB + (pc >> 3) * (kBK * 128) + rr * 128 + (((pc & 7) ^ (rr & 7)) << 4);
                             cp_async_16(dst, sr >= 0 ? static_cast<const void*>(p.gb.ptr + sr * p.gb.ld + mn) : p.gb.ptr,
                                         sr >= 0 ? 16u : 0u);
