@@ -463,7 +463,7 @@ def run_gg(args, cfg):
             orc.build()
             ro = orc.route(host["ids"], T, k, E)
             rng = np.random.default_rng(99)
-            dt, fl, desc = oracle_sample(cfg, host, ro, args.ref_rows, rng)
+            dt, fl, desc = oracle_sample(cfg, host, ro, args.cpu_rows, rng)
             line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s",
                                     "cores": orc.num_threads(), "kind": "oracle", "sample": desc,
                                     "seconds": dt}
@@ -479,7 +479,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gg", choices=["gg", "reference"])
     ap.add_argument("--config", default="mlp8")
-    ap.add_argument("--ref-rows", type=int, default=96)
+    ap.add_argument("--ref-rows", type=int, default=128,
+                    help="oracle rows per pass in each step of the reference arm")
+    ap.add_argument("--cpu-rows", type=int, default=640,
+                    help="oracle rows per pass in the cpu_baseline sample (about 10 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     from unpermute_route_hist_gb300 import synth

@@ -69,6 +69,15 @@ const char* gg_device_status_string(int code);
 /* Text of the last CUDA error seen by a host call on this thread. */
 const char* gg_last_cuda_error(void);
 
+/* Diagnostic: runs, in one CTA, the bounded mbarrier wait that every
+ * pipelined kernel of this library uses, on a barrier phase nothing ever
+ * completes, with a limit of limit_ns (0 < limit_ns <= 2 s).  The wait gives
+ * up, sets *status to GG_DEV_TIMEOUT (if it was 0) and writes *result = 0
+ * (1 would mean the phase completed).  status and result are device int32s.
+ * Lets a caller check that a stuck wait ends with an error status instead of
+ * a hang, leaving the context usable.  No counterpart on the pages. */
+int gg_selftest_bounded_wait(int32_t* status, int32_t* result, uint64_t limit_ns, void* stream);
+
 /* ------------------------------------------------------------------ route --
  * Routing metadata from the router's choices ([U] grouped_gemm_forward
  * docstring: m_sizes = tokens per expert, gather_indices sliced by

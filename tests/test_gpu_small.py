@@ -169,7 +169,10 @@ def test_backward_dX(shape, px, py):
     ref = orc.backward_dX(dY, W, ro["m_sizes"], ro["gather_idx"], T, topk, px, py)
     assert_close(hbf(dX), ref, "dX px=%d py=%d" % (px, py))
     if px:
-        assert_close(hbf(res[1]), orc.topk_sum(hbf(dX), T, topk), "dX token sum")
+        # the oracle sums its own rounded rows; each term may differ by one rounding step
+        own = orc.round_bf16(ref)
+        mag = np.abs(orc.widen_bf16(own)).reshape(T, topk, K).sum(axis=1)
+        assert_close(hbf(res[1]), orc.topk_sum(own, T, topk), "dX token sum (oracle rows)", magnitude=mag)
 
 
 @pytest.mark.parametrize("shape", SHAPES)

@@ -23,6 +23,7 @@ SIGNATURES = {
     "gg_status_string": (_cstr, [_int]),
     "gg_device_status_string": (_cstr, [_int]),
     "gg_last_cuda_error": (_cstr, []),
+    "gg_selftest_bounded_wait": (_int, [_vp, _vp, ctypes.c_uint64, _vp]),
     "gg_route_workspace_size": (_sz, [_i64, _int, _int]),
     "gg_route_hist_offsets": (_int, [_vp, _i64, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                      _vp, _vp]),

@@ -92,6 +92,27 @@ bool encode_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, u
 
 }  // namespace gg
 
+namespace gg {
+namespace {
+// One CTA waits, through the same bounded wait every pipelined kernel uses,
+// on an mbarrier phase that can never complete (nothing arrives on it).
+__global__ void selftest_wait_kernel(int32_t* status, uint64_t limit_ns, int32_t* result) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const bool ok = mbar_wait(&bar, 0, &abort_flag, status, 0, limit_ns);
+        *result = ok ? 1 : 0;
+    }
+}
+}  // namespace
+}  // namespace gg
+
 using namespace gg;
 
 namespace {
@@ -176,6 +197,14 @@ int gg_unpermute_combine(const gg_bf16* Y, const int32_t* row_id_map, const floa
     if (!al16(Y) || !al16(out)) return GG_ERR_UNSUPPORTED;
     return check_launch(
         combine_launch(Y, row_id_map, topk_w, T, topk, N, out, status, as_stream(stream)));
+}
+
+int gg_selftest_bounded_wait(int32_t* status, int32_t* result, uint64_t limit_ns, void* stream) {
+    if (!status || !result || limit_ns == 0 || limit_ns > kWaitLimitNs) return GG_ERR_INVALID_ARG;
+    selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(status, limit_ns, result);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+    return GG_OK;
 }
 
 }  // extern "C"

@@ -74,7 +74,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // time (an epilogue waiting for a whole tile), so the polling warp leaves its
 // issue slots to the warps doing the work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status, uint32_t sleep_ns = 0) {
+                                          int32_t* status, uint32_t sleep_ns = 0,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     uint32_t n = 0;
@@ -83,7 +84,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
         if (mbar_try_wait(bar, parity)) return true;
         if ((++n & 31u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 set_status(status, GG_DEV_TIMEOUT);
                 return false;

@@ -104,23 +104,27 @@ __device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
                                                 const int32_t* s_off, const int32_t* s_tp) {
     TileInfo ti;
     if (KIND == KIND_RAGGED_M) {
+        // Tiles of expert e occupy [s_tp[e]*nt_total, s_tp[e+1]*nt_total).  Inside
+        // an expert, its m-tiles are split into near-equal groups of at most
+        // kGroupM; a group sweeps every n-tile with m fastest, so W[e]'s tiles
+        // are shared by the group's CTAs in L2 and no group spans two experts.
         const int nt_total = (p.N + kBN - 1) / kBN;
-        const int mt_total = s_tp[p.E];
-        const int64_t per_group = static_cast<int64_t>(kGroupM) * nt_total;
-        const int group = static_cast<int>(t / per_group);
-        const int first = group * kGroupM;
-        const int gsize = min(mt_total - first, kGroupM);
-        const int loc = static_cast<int>(t - group * per_group);
-        const int mt = first + loc % gsize;
-        const int nt = loc / gsize;
-        // largest e with s_tp[e] <= mt
-        int lo = 0, hi = p.E - 1;
+        const int mt_glob = static_cast<int>(t / nt_total);
+        int lo = 0, hi = p.E - 1;  // largest e with s_tp[e] <= mt_glob
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (s_tp[mid] <= mt) lo = mid; else hi = mid - 1;
+            if (s_tp[mid] <= mt_glob) lo = mid; else hi = mid - 1;
         }
         const int e = lo;
-        const int lmt = mt - s_tp[e];
+        const int mt_e = s_tp[e + 1] - s_tp[e];
+        const int loc = static_cast<int>(t - static_cast<int64_t>(s_tp[e]) * nt_total);
+        const int ngroups = (mt_e + kGroupM - 1) / kGroupM;
+        const int gh = (mt_e + ngroups - 1) / ngroups;  // group height
+        const int group = loc / (gh * nt_total);
+        const int gsize = min(gh, mt_e - group * gh);
+        const int gl = loc - group * gh * nt_total;
+        const int lmt = group * gh + gl % gsize;
+        const int nt = gl / gsize;
         const int me = s_off[e + 1] - s_off[e];
         ti.e = e;
         ti.row0 = static_cast<int64_t>(s_off[e]) + static_cast<int64_t>(lmt) * kBM;
