@@ -75,6 +75,19 @@ def _dist():
     return ws, rank, local
 
 
+def aggregate_step_time(ms_local: float, flops_per_rank: float, world_size: int, dist=None,
+                        device=None):
+    """Whole-job timing of independent replicas: the slowest rank's time, and
+    throughput = all ranks' FLOPs / that time (TFLOP/s).  Returns (ms, value)."""
+    ms = float(ms_local)
+    if world_size > 1 and dist is not None:
+        import torch
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, flops_per_rank * world_size / (ms * 1e-3) / 1e12
+
+
 def _gemm_passes(cfg):
     R, K, N1, I = cfg.R, cfg.K, cfg.N1, cfg.I
     f1 = 2.0 * R * N1 * K
@@ -346,12 +359,8 @@ def run_gg(args, cfg):
         for i, n in enumerate(ev_names):
             per[n] += evs[s][i].elapsed_time(evs[s][i + 1])
     per = {n: v / args.steps for n, v in per.items()}
-    if ws > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
-    ms_step = ms_total / args.steps
-    value = step_flops * ws / (ms_step * 1e-3) / 1e12
+    ms_step, value = aggregate_step_time(ms_total / args.steps, step_flops, ws,
+                                         dist if ws > 1 else None, dev)
 
     # ---- end to end through the public API with host buffers ------------------
     pin = {n: pinned(v) for n, v in inputs_host.items()}
@@ -382,12 +391,8 @@ def run_gg(args, cfg):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1) / e_steps
-    if ws > 1:
-        tt = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e_ms = float(tt.item())
-    e_value = step_flops * ws / (e_ms * 1e-3) / 1e12
+    e_ms, e_value = aggregate_step_time(e0.elapsed_time(e1) / e_steps, step_flops, ws,
+                                        dist if ws > 1 else None, dev)
 
     # ---- the same passes with the gather fused into the GEMM (outside the step) -
     def time_call(fn, reps=3):
