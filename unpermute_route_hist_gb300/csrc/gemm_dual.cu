@@ -55,10 +55,10 @@ extern "C" int gg_dual_asym(const gg_bf16* X0, const gg_bf16* X1, const gg_bf16*
     const int64_t bound = ((m0 + kBM - 1) / kBM) * ((n0 + kBN - 1) / kBN) +
                           ((m1 + kBM - 1) / kBM) * ((n1 + kBN - 1) / kBN);
     if (trans_a && trans_b)
-        return launch_gemm<KIND_DUAL, true, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
+        return launch_gemm<KIND_DUAL, true, false, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
     if (trans_a)
-        return launch_gemm<KIND_DUAL, true, true, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
+        return launch_gemm<KIND_DUAL, true, true, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
     if (trans_b)
-        return launch_gemm<KIND_DUAL, false, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
-    return launch_gemm<KIND_DUAL, false, true, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
+        return launch_gemm<KIND_DUAL, false, false, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
+    return launch_gemm<KIND_DUAL, false, true, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, bound, st);
 }

@@ -51,10 +51,10 @@ extern "C" int gg_backward_dW(const gg_bf16* X, const gg_bf16* dY, const int32_t
     else if (!encode_map_2d(&mB, X, K, R, K, 64, kBK)) return GG_ERR_CUDA;
     const int64_t bound = static_cast<int64_t>(E) * ((N + kBM - 1) / kBM) * ((K + kBN - 1) / kBN);
     if (permute_y && permute_x)
-        return launch_gemm<KIND_RAGGED_K, true, true, true, true>(mA, mB, mA, mB, p, bound, st);
+        return launch_gemm<KIND_RAGGED_K, true, true, true, true, false>(mA, mB, mA, mB, p, bound, st);
     if (permute_y)
-        return launch_gemm<KIND_RAGGED_K, true, true, true, false>(mA, mB, mA, mB, p, bound, st);
+        return launch_gemm<KIND_RAGGED_K, true, true, true, false, false>(mA, mB, mA, mB, p, bound, st);
     if (permute_x)
-        return launch_gemm<KIND_RAGGED_K, true, true, false, true>(mA, mB, mA, mB, p, bound, st);
-    return launch_gemm<KIND_RAGGED_K, true, true, false, false>(mA, mB, mA, mB, p, bound, st);
+        return launch_gemm<KIND_RAGGED_K, true, true, false, true, false>(mA, mB, mA, mB, p, bound, st);
+    return launch_gemm<KIND_RAGGED_K, true, true, false, false, false>(mA, mB, mA, mB, p, bound, st);
 }

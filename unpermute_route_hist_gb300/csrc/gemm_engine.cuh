@@ -10,6 +10,9 @@
 // dw comment; backend.py: asym_dual_gmm_separated.)
 //
 // Tile: 128 x 256 output, reduction blocks of 64, 4-stage shared-memory ring,
+// optionally (PAIR) run by 2-CTA clusters on adjacent m-tiles that share the
+// B tile: each CTA TMA-loads half of it and multicasts it to both, and a stage
+// is released only when both CTAs' MMAs have read it;
 // fp32 accumulators in tensor memory (two 256-column buffers so the epilogue
 // of one tile overlaps the main loop of the next).  Warp roles:
 //   warp 0      tile scheduler + TMA producer (lane 0) for dense operands
@@ -17,7 +20,7 @@
 //   warps 2-5   epilogue: TMEM -> registers -> scale -> bf16 -> global rows
 //   warps 6-9   (only with a gathered operand) cp.async row-gather producers;
 //               each thread's copies arrive on the stage barrier as they land
-// Every role walks the same static tile list (tile = blockIdx.x + j*gridDim.x),
+// Every role walks the same static tile list (slot + j*nslot, per CTA or cluster),
 // decoded from m_sizes in shared memory, so no role sends tile ids to another.
 //
 // Shared-memory operand layouts are the tcgen05 canonical 128-byte-swizzle
@@ -99,31 +102,39 @@ struct SharedCtl {
     int64_t total_tiles;
 };
 
-template <int KIND>
+// Tiles are scheduled in "units": one m-tile, or (PAIR) two adjacent m-tiles
+// of the same expert / problem and n-tile that a 2-CTA cluster computes
+// together, CTA rank r taking m-tile 2*unit + r.  A rank whose m-tile falls
+// past the end gets rows <= 0 (a phantom tile: it loads and releases its half
+// of the shared operand but computes and stores nothing).
+template <int KIND, bool PAIR>
 __device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
-                                                const int32_t* s_off, const int32_t* s_tp) {
+                                                const int32_t* s_off, const int32_t* s_tp,
+                                                uint32_t rank) {
+    constexpr int U = PAIR ? 2 : 1;
+    constexpr int kGroupU = kGroupM / U;  // units per raster group
     TileInfo ti;
     if (KIND == KIND_RAGGED_M) {
-        // Tiles of expert e occupy [s_tp[e]*nt_total, s_tp[e+1]*nt_total).  Inside
-        // an expert, its m-tiles are split into near-equal groups of at most
-        // kGroupM; a group sweeps every n-tile with m fastest, so W[e]'s tiles
+        // Units of expert e occupy [s_tp[e]*nt_total, s_tp[e+1]*nt_total).  Inside
+        // an expert its units are split into near-equal groups of at most
+        // kGroupU; a group sweeps every n-tile with m fastest, so W[e]'s tiles
         // are shared by the group's CTAs in L2 and no group spans two experts.
         const int nt_total = (p.N + kBN - 1) / kBN;
-        const int mt_glob = static_cast<int>(t / nt_total);
-        int lo = 0, hi = p.E - 1;  // largest e with s_tp[e] <= mt_glob
+        const int ut_glob = static_cast<int>(t / nt_total);
+        int lo = 0, hi = p.E - 1;  // largest e with s_tp[e] <= ut_glob
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (s_tp[mid] <= mt_glob) lo = mid; else hi = mid - 1;
+            if (s_tp[mid] <= ut_glob) lo = mid; else hi = mid - 1;
         }
         const int e = lo;
-        const int mt_e = s_tp[e + 1] - s_tp[e];
+        const int ut_e = s_tp[e + 1] - s_tp[e];
         const int loc = static_cast<int>(t - static_cast<int64_t>(s_tp[e]) * nt_total);
-        const int ngroups = (mt_e + kGroupM - 1) / kGroupM;
-        const int gh = (mt_e + ngroups - 1) / ngroups;  // group height
+        const int ngroups = (ut_e + kGroupU - 1) / kGroupU;
+        const int gh = (ut_e + ngroups - 1) / ngroups;  // group height
         const int group = loc / (gh * nt_total);
-        const int gsize = min(gh, mt_e - group * gh);
+        const int gsize = min(gh, ut_e - group * gh);
         const int gl = loc - group * gh * nt_total;
-        const int lmt = group * gh + gl % gsize;
+        const int lmt = (group * gh + gl % gsize) * U + static_cast<int>(rank);
         const int nt = gl / gsize;
         const int me = s_off[e + 1] - s_off[e];
         ti.e = e;
@@ -134,19 +145,20 @@ __device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
         ti.red_len = p.Kred;
     } else if (KIND == KIND_RAGGED_K) {
         const int mt_per = (p.M + kBM - 1) / kBM;
+        const int ut_per = (mt_per + U - 1) / U;
         const int nt_per = (p.N + kBN - 1) / kBN;
-        const int64_t per_e = static_cast<int64_t>(mt_per) * nt_per;
+        const int64_t per_e = static_cast<int64_t>(ut_per) * nt_per;
         const int e = static_cast<int>(t / per_e);
         const int loc = static_cast<int>(t - e * per_e);
-        // grouped raster inside the expert: kGroupM m-tiles x every n-tile, m
+        // grouped raster inside the expert: kGroupU units x every n-tile, m
         // fastest, so concurrent CTAs share both A and B tiles in L2 and no
         // single tile is read by every SM at once
-        const int per_group = kGroupM * nt_per;
+        const int per_group = kGroupU * nt_per;
         const int group = loc / per_group;
-        const int first = group * kGroupM;
-        const int gsize = min(mt_per - first, kGroupM);
+        const int first = group * kGroupU;
+        const int gsize = min(ut_per - first, kGroupU);
         const int gl = loc - group * per_group;
-        const int mt = first + gl % gsize, nt = gl / gsize;
+        const int mt = (first + gl % gsize) * U + static_cast<int>(rank), nt = gl / gsize;
         ti.e = e;
         ti.row0 = static_cast<int64_t>(mt) * kBM;
         ti.rows = min(kBM, p.M - mt * kBM);
@@ -154,12 +166,13 @@ __device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
         ti.red0 = s_off[e];
         ti.red_len = s_off[e + 1] - s_off[e];
     } else {
-        const int mt0 = (p.dual[0].m + kBM - 1) / kBM;
-        const int64_t tiles0 = static_cast<int64_t>(mt0) * ((p.dual[0].n + kBN - 1) / kBN);
+        const int ut0 = ((p.dual[0].m + kBM - 1) / kBM + U - 1) / U;
+        const int64_t tiles0 = static_cast<int64_t>(ut0) * ((p.dual[0].n + kBN - 1) / kBN);
         const int q = t < tiles0 ? 0 : 1;
         const int64_t lt = q == 0 ? t : t - tiles0;
-        const int mtq = (p.dual[q].m + kBM - 1) / kBM;
-        const int mt = static_cast<int>(lt % mtq), nt = static_cast<int>(lt / mtq);
+        const int utq = ((p.dual[q].m + kBM - 1) / kBM + U - 1) / U;
+        const int mt = static_cast<int>(lt % utq) * U + static_cast<int>(rank);
+        const int nt = static_cast<int>(lt / utq);
         ti.e = q;
         ti.row0 = static_cast<int64_t>(mt) * kBM;
         ti.rows = min(kBM, p.dual[q].m - mt * kBM);
@@ -192,13 +205,17 @@ __device__ __forceinline__ int64_t gather_row(const GemmParams& p, const GatherS
     return r;
 }
 
-template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER>
+template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR>
 struct GemmTraits {
+    static_assert(!(PAIR && B_GATHER), "the shared (multicast) operand is loaded by TMA");
     static constexpr bool kAnyGather = A_GATHER || B_GATHER;
     static constexpr int kThreads = 32 * (6 + (kAnyGather ? kGatherWarps : 0));
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, A_MN ? 1 : 0, B_MN ? 1 : 0);
     static constexpr uint32_t kTmaBytes = (A_GATHER ? 0u : kABytes) + (B_GATHER ? 0u : kBBytes);
     static constexpr uint32_t kFullCount = 1 + (kAnyGather ? kGatherWarps * 32 : 0);
+    // a stage is free once every CTA that reads the shared operand released it
+    static constexpr uint32_t kEmptyCount = PAIR ? 2 : 1;
+    static constexpr uint16_t kPairMask = 0x3;
 };
 
 __host__ __device__ constexpr size_t gemm_smem_bytes(int E) {
@@ -220,12 +237,12 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t tile_addr, int ks) {
     }
 }
 
-template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER>
-__global__ void __launch_bounds__((GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER>::kThreads), 1)
+template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR>
+__global__ void __launch_bounds__((GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>::kThreads), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                     const GemmParams p) {
-    using Tr = GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER>;
+    using Tr = GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -236,12 +253,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
 
     const int warp = warp_id(), lane = lane_id();
     volatile int* abort_flag = &ctl->abort_flag;
+    // persistent schedule: CTAs (or 2-CTA clusters) take units slot, slot + nslot, ...
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int64_t slot = PAIR ? static_cast<int64_t>(cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
+    const int64_t nslot = PAIR ? static_cast<int64_t>(nclusters_x()) : static_cast<int64_t>(gridDim.x);
 
     // ---------------------------------------------------------- prologue --
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl->full[s], Tr::kFullCount);
-            mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->empty[s], Tr::kEmptyCount);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tmem_full[b], 1);
@@ -269,8 +290,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         int64_t total_tiles = 0;
         int bad = 0;
         if (KIND == KIND_DUAL) {
-            const int64_t t0 = static_cast<int64_t>((p.dual[0].m + kBM - 1) / kBM) * ((p.dual[0].n + kBN - 1) / kBN);
-            const int64_t t1 = static_cast<int64_t>((p.dual[1].m + kBM - 1) / kBM) * ((p.dual[1].n + kBN - 1) / kBN);
+            constexpr int U = PAIR ? 2 : 1;
+            const int64_t t0 = static_cast<int64_t>(((p.dual[0].m + kBM - 1) / kBM + U - 1) / U) * ((p.dual[0].n + kBN - 1) / kBN);
+            const int64_t t1 = static_cast<int64_t>(((p.dual[1].m + kBM - 1) / kBM + U - 1) / U) * ((p.dual[1].n + kBN - 1) / kBN);
             total_tiles = t0 + t1;
         } else {
             const int seg = (p.E + 31) / 32;
@@ -281,7 +303,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 const int m = p.m_sizes[e];
                 if (m < 0) bad = 1;
                 rsum += m > 0 ? m : 0;
-                tsum += m > 0 ? (m + kBM - 1) / kBM : 0;
+                tsum += m > 0 ? ((m + kBM - 1) / kBM + (PAIR ? 1 : 0)) / (PAIR ? 2 : 1) : 0;
             }
             int64_t rx = rsum;
             int tx = tsum;
@@ -297,7 +319,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 s_off[e] = static_cast<int32_t>(rrun);
                 s_tp[e] = trun;
                 rrun += m;
-                trun += (m + kBM - 1) / kBM;
+                trun += ((m + kBM - 1) / kBM + (PAIR ? 1 : 0)) / (PAIR ? 2 : 1);
             }
             const int64_t rtot = __shfl_sync(0xffffffffu, rx, 31);
             const int ttot = __shfl_sync(0xffffffffu, tx, 31);
@@ -310,7 +332,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             if (KIND == KIND_RAGGED_M) {
                 total_tiles = static_cast<int64_t>(ttot) * ((p.N + kBN - 1) / kBN);
             } else {
-                total_tiles = static_cast<int64_t>(p.E) * ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
+                total_tiles = static_cast<int64_t>(p.E) * (((p.M + kBM - 1) / kBM + (PAIR ? 1 : 0)) / (PAIR ? 2 : 1)) *
+                              ((p.N + kBN - 1) / kBN);
             }
         }
         if (lane == 0) {
@@ -321,6 +344,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     }
     tc_fence_before();
     __syncthreads();
+    // the partner CTA's barriers must be initialised before any multicast
+    // copy or remote arrival reaches them
+    if (PAIR) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     const int64_t total_tiles = ctl->total_tiles;
@@ -333,18 +359,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile<KIND>(t, p, s_off, s_tp);
+            for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
+                const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
                 const CUtensorMap* mA = (KIND == KIND_DUAL && ti.e == 1) ? &tmA1 : &tmA0;
                 const CUtensorMap* mB = (KIND == KIND_DUAL && ti.e == 1) ? &tmB1 : &tmB0;
+                const bool phantom = ti.rows <= 0;
+                const uint32_t tx = (A_GATHER || phantom ? 0u : static_cast<uint32_t>(kABytes)) +
+                                    (B_GATHER ? 0u : static_cast<uint32_t>(kBBytes));
                 for (int kb = 0; kb < ti.nkb; ++kb) {
                     if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     uint8_t* sA = stage_base + stage * kStageBytes;
                     uint8_t* sB = sA + kABytes;
-                    if (Tr::kTmaBytes) mbar_arrive_expect_tx(&ctl->full[stage], Tr::kTmaBytes);
+                    if (tx) mbar_arrive_expect_tx(&ctl->full[stage], tx);
                     else mbar_arrive(&ctl->full[stage]);
                     const int32_t red = static_cast<int32_t>(ti.red0 + static_cast<int64_t>(kb) * kBK);
-                    if (!A_GATHER) {
+                    if (!A_GATHER && !phantom) {
                         if (!A_MN) {
                             tma_load_2d(sA, mA, &ctl->full[stage], red, static_cast<int32_t>(ti.row0));
                         } else {
@@ -355,7 +384,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         }
                     }
                     if (!B_GATHER) {
-                        if (!B_MN) {
+                        if (PAIR) {
+                            // this CTA loads half of the shared B tile into both CTAs
+                            if (!B_MN) {
+                                uint8_t* dst = sB + rank * (kBBytes / 2);
+                                const int32_t n = ti.n0 + static_cast<int32_t>(rank) * (kBN / 2);
+                                if (KIND == KIND_RAGGED_M)
+                                    tma_load_3d_mc(dst, mB, &ctl->full[stage], red, n, ti.e, Tr::kPairMask);
+                                else
+                                    tma_load_2d_mc(dst, mB, &ctl->full[stage], red, n, Tr::kPairMask);
+                            } else {
+#pragma unroll
+                                for (int h = 0; h < kBN / 128; ++h) {
+                                    const int cc = static_cast<int>(rank) * (kBN / 128) + h;
+                                    if (KIND == KIND_RAGGED_M)
+                                        tma_load_3d_mc(sB + cc * kBK * 128, mB, &ctl->full[stage],
+                                                       ti.n0 + cc * 64, red, ti.e, Tr::kPairMask);
+                                    else
+                                        tma_load_2d_mc(sB + cc * kBK * 128, mB, &ctl->full[stage],
+                                                       ti.n0 + cc * 64, red, Tr::kPairMask);
+                                }
+                            }
+                        } else if (!B_MN) {
                             if (KIND == KIND_RAGGED_M)
                                 tma_load_3d(sB, mB, &ctl->full[stage], red, ti.n0, ti.e);
                             else
@@ -378,10 +428,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             }
             // Let every TMA copy this thread issued land before the CTA can exit.
             const int64_t pend = issued < kStages ? issued : kStages;
+            int dstage = stage;
+            uint32_t dphase = phase;
             for (int64_t j = 0; j < pend; ++j) {
-                if (--stage < 0) { stage = kStages - 1; phase ^= 1u; }
+                if (--dstage < 0) { dstage = kStages - 1; dphase ^= 1u; }
                 int dummy = 0;
-                mbar_wait(&ctl->full[stage], phase, reinterpret_cast<volatile int*>(&dummy), p.status);
+                mbar_wait(&ctl->full[dstage], dphase, reinterpret_cast<volatile int*>(&dummy), p.status);
+            }
+            // With a partner CTA: acquire every slot once more, i.e. wait until both
+            // CTAs released each stage, so no remote arrival can reach this CTA's
+            // barriers after it exits.
+            if (PAIR && issued > 0) {
+                for (int j = 0; j < kStages; ++j) {
+                    int dummy = 0;
+                    mbar_wait(&ctl->empty[stage], phase ^ 1u, reinterpret_cast<volatile int*>(&dummy), p.status);
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
             }
         }
     } else if (warp == 1) {
@@ -390,9 +452,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         uint32_t phase = 0;
         uint32_t acc_count = 0;
         bool ok = true, any_mma = false;
-        for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-            const TileInfo ti = decode_tile<KIND>(t, p, s_off, s_tp);
+        for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
+            const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
             if (ti.nkb == 0) continue;
+            if (PAIR && ti.rows <= 0) {
+                // phantom tile: only release each stage to both CTAs once it landed
+                for (int kb = 0; kb < ti.nkb; ++kb) {
+                    if (!warp_wait(&ctl->full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+                    if (lane == 0) {
+                        mbar_arrive_cluster(&ctl->empty[stage], 0);
+                        mbar_arrive_cluster(&ctl->empty[stage], 1);
+                    }
+                    __syncwarp();
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+                continue;
+            }
             const uint32_t buf = acc_count & 1u;
             const uint32_t acc_phase = (acc_count >> 1) & 1u;
             if (!warp_wait(&ctl->tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
@@ -441,7 +516,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         umma_bf16(d_tmem, operand_desc<A_MN>(sA, ks), operand_desc<B_MN>(sB, ks),
                                   Tr::kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
                     }
-                    umma_commit(&ctl->empty[stage]);
+                    if (PAIR) umma_commit_mc(&ctl->empty[stage], Tr::kPairMask);
+                    else umma_commit(&ctl->empty[stage]);
                     any_mma = true;
                 }
                 __syncwarp();
@@ -464,8 +540,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         const int q = warp & 3;        // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;   // tile row of this thread
         uint32_t acc_count = 0;
-        for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-            const TileInfo ti = decode_tile<KIND>(t, p, s_off, s_tp);
+        for (int64_t t = slot; t < total_tiles; t += nslot) {
+            const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
+            if (ti.rows <= 0) continue;  // phantom tile: nothing to store
             const int ncols = tile_cols<KIND>(p, ti.e);
             // destination row, scale, output base
             uint16_t* out = p.out;
@@ -548,7 +625,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
 #pragma unroll
                 for (int j = 0; j < 8; ++j) a_next[j] = -1;
                 if (tt < total_tiles) {
-                    const TileInfo tn = decode_tile<KIND>(tt, p, s_off, s_tp);
+                    const TileInfo tn = decode_tile<KIND, PAIR>(tt, p, s_off, s_tp, rank);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int rr = (gt >> 3) + 16 * j;
@@ -575,9 +652,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 if (r >= g.rows) { set_status(p.status, GG_DEV_BAD_ROW_INDEX); return -1; }
                 return r;
             };
-            if (A_GATHER && !A_MN) fetch_a_rows(blockIdx.x);
-            for (int64_t t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile<KIND>(t, p, s_off, s_tp);
+            if (A_GATHER && !A_MN) fetch_a_rows(slot);
+            for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
+                const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
                 const uint16_t* arow[8];
                 if (A_GATHER && !A_MN) {
 #pragma unroll
@@ -585,7 +662,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         const int64_t sr = src_row(p.ga, a_next[j]);
                         arow[j] = sr >= 0 ? p.ga.ptr + sr * p.ga.ld : nullptr;
                     }
-                    fetch_a_rows(t + gridDim.x);
+                    fetch_a_rows(t + nslot);
                 }
                 constexpr bool kRedGather = (A_GATHER && A_MN) || B_GATHER;
                 if (kRedGather) {
@@ -665,6 +742,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     // ----------------------------------------------------------- teardown --
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync();  // neither CTA leaves while the other may still signal it
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
@@ -678,18 +756,53 @@ bool encode_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, u
 int num_sms();
 void record_cuda_error(cudaError_t e);
 
-template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER>
+template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR>
 int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
                 const CUtensorMap& b1, const GemmParams& p, int64_t tile_bound, cudaStream_t stream) {
-    using Tr = GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER>;
-    auto kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER>;
+    using Tr = GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>;
+    auto kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>;
     const size_t smem = gemm_smem_bytes(p.E);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(gemm_smem_bytes(GG_MAX_EXPERTS)));
     if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
     const int64_t sms = num_sms();
-    const int64_t grid = tile_bound < sms ? (tile_bound > 0 ? tile_bound : 1) : sms;
-    kern<<<static_cast<unsigned>(grid), Tr::kThreads, smem, stream>>>(a0, b0, a1, b1, p);
+    if (tile_bound < 1) tile_bound = 1;
+    if (!PAIR) {
+        const int64_t grid = tile_bound < sms ? tile_bound : sms;
+        kern<<<static_cast<unsigned>(grid), Tr::kThreads, smem, stream>>>(a0, b0, a1, b1, p);
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(Tr::kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // as many 2-CTA clusters as can be resident at once (a GPC with an odd
+        // SM count leaves an SM out), at most one per tile pair
+        static int max_clusters[64] = {0};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 0 || dev >= 64) dev = 0;
+        if (max_clusters[dev] == 0) {
+            cfg.gridDim = dim3(static_cast<unsigned>(sms & ~int64_t(1)));
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            if (e != cudaSuccess || n < 1) {
+                record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidConfiguration);
+                return GG_ERR_CUDA;
+            }
+            max_clusters[dev] = n;
+        }
+        const int64_t clusters = tile_bound < max_clusters[dev] ? tile_bound : max_clusters[dev];
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+        e = cudaLaunchKernelEx(&cfg, kern, a0, b0, a1, b1, p);
+        if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
     return GG_OK;

@@ -70,10 +70,10 @@ int gg_forward(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
     if (permute_x) {
         p.ga = GatherSrc{X, K, T, K, ROW_TOKEN};
         mA = mB;  // unused
-        return launch_gemm<KIND_RAGGED_M, false, false, true, false>(mA, mB, mA, mB, p, bound, st);
+        return launch_gemm<KIND_RAGGED_M, false, false, true, false, false>(mA, mB, mA, mB, p, bound, st);
     }
     if (!encode_map_2d(&mA, X, K, R, K, kBK, kBM)) return GG_ERR_CUDA;
-    return launch_gemm<KIND_RAGGED_M, false, false, false, false>(mA, mB, mA, mB, p, bound, st);
+    return launch_gemm<KIND_RAGGED_M, false, false, false, false, false>(mA, mB, mA, mB, p, bound, st);
 }
 
 int gg_backward_dX(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes,
@@ -108,10 +108,10 @@ int gg_backward_dX(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes,
         const int64_t bound = row_tile_bound(R, E) * ((K + kBN - 1) / kBN);
         if (permute_y) {
             p.ga = GatherSrc{dY, N, R, N, ROW_SLOT};
-            rc = launch_gemm<KIND_RAGGED_M, false, true, true, false>(mB, mB, mB, mB, p, bound, st);
+            rc = launch_gemm<KIND_RAGGED_M, false, true, true, false, false>(mB, mB, mB, mB, p, bound, st);
         } else {
             if (!encode_map_2d(&mA, dY, N, R, N, kBK, kBM)) return GG_ERR_CUDA;
-            rc = launch_gemm<KIND_RAGGED_M, false, true, false, false>(mA, mB, mA, mB, p, bound, st);
+            rc = launch_gemm<KIND_RAGGED_M, false, true, false, false, false>(mA, mB, mA, mB, p, bound, st);
         }
     }
     if (rc != GG_OK || !dX_tok) return rc;
