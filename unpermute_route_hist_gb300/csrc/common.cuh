@@ -276,20 +276,22 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle.
+// Shared-memory matrix descriptor for tcgen05.mma.
 //   bits  0-13  start address >> 4
 //   bits 16-29  leading-dimension byte offset >> 4
 //   bits 32-45  stride-dimension byte offset >> 4
 //   bits 46-47  descriptor version (1 on this architecture)
-//   bits 61-63  layout: 2 = 128-byte swizzle
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes) {
+//   bits 61-63  layout: 2 = 128-byte swizzle, 4 = 64-byte swizzle
+constexpr uint32_t kLayoutSw128 = 2;
+constexpr uint32_t kLayoutSw64 = 4;
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t layout) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
     d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
+    d |= static_cast<uint64_t>(layout) << 61;
     return d;
 }
 

@@ -9,7 +9,7 @@
 // (interface.py: grouped_gemm_forward / _dX / _dW; matmul_ogs.py: the ragged
 // dw comment; backend.py: asym_dual_gmm_separated.)
 //
-// Tile: 128 x 256 output, reduction blocks of 64, 4-stage shared-memory ring,
+// Tile: 128 x 256 output, reduction blocks of kBK, a kStages-deep shared-memory ring,
 // optionally (PAIR) run by 2-CTA clusters on adjacent m-tiles that share the
 // B tile: each CTA TMA-loads half of it and multicasts it to both, and a stage
 // is released only when both CTAs' MMAs have read it;
@@ -23,11 +23,12 @@
 // Every role walks the same static tile list (slot + j*nslot, per CTA or cluster),
 // decoded from m_sizes in shared memory, so no role sends tile ids to another.
 //
-// Shared-memory operand layouts are the tcgen05 canonical 128-byte-swizzle
-// layouts: K-major tiles are rows of 64 bf16 (128 B), 8-row atoms of 1 KB;
-// MN-major tiles are 64-element MN chunks, each BK reduction rows of 128 B.
-// TMA with 128-byte swizzle writes exactly these; the gather producers write
-// the same swizzle by hand (16-byte chunk c of row r goes to c ^ (r & 7)).
+// Shared-memory operand layouts are the tcgen05 canonical swizzled layouts:
+// K-major tiles are rows of kBK bf16 with a swizzle as wide as the row (64-
+// or 128-byte), 8-row atoms; MN-major tiles are 64-element MN chunks, each kBK
+// reduction rows of 128 B with the 128-byte swizzle.  TMA with the matching
+// swizzle writes exactly these; the gather producers write the same swizzle by
+// hand (kmajor_chunk_offset, and chunk c of an MN row r at c ^ (r & 7)).
 #pragma once
 
 #include "common.cuh"
@@ -36,10 +37,13 @@ namespace gg {
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;
-constexpr int kBK = 64;
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;  // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
+constexpr int kBK = 64;                  // reduction block (32 or 64)
+constexpr int kStages = 4;               // 192 KB of operand stages
+// K-major tiles: rows of kBK bf16 (kKRowBytes), swizzled over the row width
+constexpr int kKRowBytes = kBK * 2;
+constexpr int kKChunks = kKRowBytes / 16;  // 16-byte chunks per K-major row
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators
 constexpr int kGroupM = 16;             // m-tiles per raster group (L2 reuse)
@@ -223,17 +227,27 @@ __host__ __device__ constexpr size_t gemm_smem_bytes(int E) {
            sizeof(SharedCtl) + 2 * static_cast<size_t>(E + 1) * sizeof(int32_t) + 16;
 }
 
+// Byte offset of 16-byte chunk c of row r in a K-major tile: the swizzle XORs
+// the chunk index with address bits 7.. (128-byte rows: r & 7; 64-byte rows:
+// (r >> 1) & 3), matching TMA's 128-/64-byte swizzle of the same tile.
+__host__ __device__ constexpr uint32_t kmajor_chunk_offset(int r, int c) {
+    return kKRowBytes == 128 ? static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4))
+                             : static_cast<uint32_t>(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
 // Shared-memory descriptor of k-step `ks` (16 reduction elements) of an operand tile.
 template <bool MN_MAJOR>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t tile_addr, int ks) {
     if (MN_MAJOR) {
         // MN chunks of 64 elements are kBK*128 bytes apart (leading offset);
         // 8-row reduction groups are 1 KB apart (stride offset); a k-step is
-        // 16 reduction rows = 2 KB further.
-        return smem_desc_sw128(tile_addr + ks * 2048, kBK * 128, 1024);
+        // 16 reduction rows = 2 KB further.  128-byte swizzle.
+        return smem_desc(tile_addr + ks * 2048, kBK * 128, 1024, kLayoutSw128);
     } else {
-        // rows of 128 B, 8-row atoms 1 KB apart; a k-step is 32 B along the row.
-        return smem_desc_sw128(tile_addr + ks * 32, 16, 1024);
+        // rows of kKRowBytes, 8-row atoms 8*kKRowBytes apart; a k-step is 32 B
+        // along the row.  Swizzle span = row width.
+        return smem_desc(tile_addr + ks * 32, 16, 8 * kKRowBytes,
+                         kKRowBytes == 128 ? kLayoutSw128 : kLayoutSw64);
     }
 }
 
@@ -619,29 +633,41 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            // K-major gathered A: the tile's 8 rows of this thread (fixed over the tile).
-            int32_t a_next[8];
+            // K-major gathered A: thread gt copies chunk gt % kKChunks of rows
+            // gt / kKChunks + kARowStep * j (fixed over the tile).
+            constexpr int kARowStep = 128 / kKChunks;
+            constexpr int kARows = kBM / kARowStep;
+            int32_t a_next[kARows];
             auto fetch_a_rows = [&](int64_t tt) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) a_next[j] = -1;
+                for (int j = 0; j < kARows; ++j) a_next[j] = -1;
                 if (tt < total_tiles) {
                     const TileInfo tn = decode_tile<KIND, PAIR>(tt, p, s_off, s_tp, rank);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int rr = (gt >> 3) + 16 * j;
+                    for (int j = 0; j < kARows; ++j) {
+                        const int rr = gt / kKChunks + kARowStep * j;
                         if (rr < tn.rows) a_next[j] = p.gather_idx[tn.row0 + rr];
                     }
                 }
             };
-            // MN-major gathered operands (dW): the 64 slot numbers of a stage are
-            // loaded cooperatively (lane L holds rows 2L and 2L+1) three stages
-            // before use, then handed to the threads that copy each row by shuffle.
-            const int glane = gt & 31, gw = gt >> 5;
+            // MN-major gathered operands (dW): the kBK slot numbers of a stage are
+            // loaded cooperatively (lane L holds rows kIPL*L .. kIPL*L+kIPL-1) three
+            // stages before use, then handed to the copying threads by shuffle.
+            constexpr int kIPL = kBK / 32;  // slot numbers per lane (1 or 2)
+            const int glane = gt & 31;
             int32_t q_lo[4], q_hi[4];  // look-ahead ring, fully unrolled rotation below
             auto load_stage_idx = [&](const TileInfo& tn, int kb, int32_t& lo, int32_t& hi) {
-                const int64_t k0 = static_cast<int64_t>(kb) * kBK + 2 * glane;
+                const int64_t k0 = static_cast<int64_t>(kb) * kBK + kIPL * glane;
                 lo = (kb < tn.nkb && k0 < tn.red_len) ? p.gather_idx[tn.red0 + k0] : -1;
-                hi = (kb < tn.nkb && k0 + 1 < tn.red_len) ? p.gather_idx[tn.red0 + k0 + 1] : -1;
+                hi = (kIPL == 2 && kb < tn.nkb && k0 + 1 < tn.red_len) ? p.gather_idx[tn.red0 + k0 + 1] : -1;
+            };
+            // slot number of reduction row rr of the current stage.  Full-warp
+            // shuffles: every lane must call it, whatever its own row or column
+            // validity (a lane that skipped it would leave the warp waiting).
+            auto stage_slot = [&](int32_t lo, int32_t hi, int rr) -> int32_t {
+                const int32_t l = __shfl_sync(0xffffffffu, lo, rr / kIPL);
+                const int32_t h = __shfl_sync(0xffffffffu, hi, rr / kIPL);
+                return (kIPL == 2 && (rr & 1)) ? h : l;
             };
             // slot number -> source row of a gathered operand, -1 if absent or out of range
             auto src_row = [&](const GatherSrc& g, int32_t f) -> int64_t {
@@ -655,10 +681,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             if (A_GATHER && !A_MN) fetch_a_rows(slot);
             for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
                 const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
-                const uint16_t* arow[8];
+                const uint16_t* arow[kARows];
                 if (A_GATHER && !A_MN) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < kARows; ++j) {
                         const int64_t sr = src_row(p.ga, a_next[j]);
                         arow[j] = sr >= 0 ? p.ga.ptr + sr * p.ga.ld : nullptr;
                     }
@@ -684,28 +710,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     }
                     if (A_GATHER) {
                         if (!A_MN) {
-                            const int c = gt & 7;
+                            const int c = gt % kKChunks;
                             const int64_t col = static_cast<int64_t>(kb) * kBK + c * 8;
                             const bool cv = col < p.ga.cols;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const int rr = (gt >> 3) + 16 * j;
-                                const uint32_t dst = sA + rr * 128 + ((c ^ (rr & 7)) << 4);
+                            for (int j = 0; j < kARows; ++j) {
+                                const int rr = gt / kKChunks + kARowStep * j;
+                                const uint32_t dst = sA + kmajor_chunk_offset(rr, c);
                                 const bool v = cv && arow[j] != nullptr;
                                 cp_async_16(dst, v ? static_cast<const void*>(arow[j] + col) : p.ga.ptr, v ? 16u : 0u);
                             }
                         } else {
                             // MN-major: reduction rows are gathered rows; 16 pieces of 8 elements per row.
-                            // Row rr = 2*gw + (glane >> 4) + 8j sits in lane rr >> 1 = gw + 4j.
                             const int pc = gt & 15;
                             const int64_t mn = ti.row0 + pc * 8;
                             const bool mv = mn < p.ga.cols;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
+                            for (int j = 0; j < kBK / 8; ++j) {
                                 const int rr = (gt >> 4) + 8 * j;
-                                const int32_t lo = __shfl_sync(0xffffffffu, cur_lo, gw + 4 * j);
-                                const int32_t hi = __shfl_sync(0xffffffffu, cur_hi, gw + 4 * j);
-                                const int64_t sr = mv ? src_row(p.ga, (glane >> 4) ? hi : lo) : -1;
+                                const int32_t f = stage_slot(cur_lo, cur_hi, rr);  // every lane shuffles
+                                const int64_t sr = mv ? src_row(p.ga, f) : -1;
                                 const uint32_t dst = sA + (pc >> 3) * (kBK * 128) + rr * 128 + (((pc & 7) ^ (rr & 7)) << 4);
                                 cp_async_16(dst, sr >= 0 ? static_cast<const void*>(p.ga.ptr + sr * p.ga.ld + mn) : p.ga.ptr,
                                             sr >= 0 ? 16u : 0u);
@@ -717,12 +741,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         const int pc = gt & 31;
                         const int64_t mn = static_cast<int64_t>(ti.n0) + pc * 8;
                         const bool mv = mn < p.gb.cols;
-                        // Row rr = gw + 4j sits in lane rr >> 1, in its low or high slot by gw & 1.
-                        const int32_t sel = (gw & 1) ? cur_hi : cur_lo;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
+                        for (int j = 0; j < kBK / 4; ++j) {
                             const int rr = (gt >> 5) + 4 * j;
-                            const int32_t f = __shfl_sync(0xffffffffu, sel, (gw + 4 * j) >> 1);
+                            const int32_t f = stage_slot(cur_lo, cur_hi, rr);  // every lane shuffles
                             const int64_t sr = mv ? src_row(p.gb, f) : -1;
                             const uint32_t dst = sB + (pc >> 3) * (kBK * 128) + rr * 128 + (((pc & 7) ^ (rr & 7)) << 4);
                             cp_async_16(dst, sr >= 0 ? static_cast<const void*>(p.gb.ptr + sr * p.gb.ld + mn) : p.gb.ptr,
