@@ -68,6 +68,28 @@ def _peak_value(d, keys, default):
     return default
 
 
+def _roofline_traffic():
+    """Per-launch DRAM bytes of the roofline kernel from the committed ncu
+    summary, or None once the engine source differs from the captured one."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
+    eng = os.path.join(ROOT, "unpermute_route_hist_gb300", "csrc", "gemm_engine.cuh")
+    try:
+        kv = {}
+        with open(path) as fh:
+            for line in fh:
+                if "=" in line and not line.startswith("#"):
+                    k, v = (x.strip() for x in line.split("=", 1))
+                    kv[k] = v
+        with open(eng, "rb") as fh:
+            sha = hashlib.sha256(fh.read()).hexdigest()
+        if not sha.startswith(kv["engine_sha256_prefix"]):
+            return None
+        return int(kv["dram_bytes_read"]) + int(kv["dram_bytes_write"])
+    except Exception:
+        return None
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -434,6 +456,7 @@ def run_gg(args, cfg):
     if rank == 0:
         peaks, src_kind = _peaks()
         tflops_sus = _peak_value(peaks, ["bf16_tflops_sustained", "bf16_tflops"], 1700.0)
+        tflops_burst = _peak_value(peaks, ["bf16_tflops"], 1900.0)
         hbm = _peak_value(peaks, ["hbm_gbs", "hbm_GBs", "hbm"], 6800.0)
         dom = "fwd1"
         achieved = passes[dom] / (per[dom] * 1e-3) / 1e12
@@ -446,7 +469,9 @@ def run_gg(args, cfg):
             "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (GEMM1 forward, dense TMA operands)",
                          "achieved": achieved, "peak": tflops_sus, "unit": "TFLOP/s",
                          "frac": achieved / tflops_sus, "peak_source": src_kind + " bf16 sustained",
-                         "traffic": None},
+                         "frac_of_burst_peak": achieved / tflops_burst, "burst_peak": tflops_burst,
+                         "traffic": _roofline_traffic(), "traffic_unit": "bytes per launch",
+                         "algorithmic_bytes": (R * K + E * N1 * K + R * N1) * 2},
             "gemm": {"tflops_all_gemm_launches": sum(passes.values()) / (gemm_ms * 1e-3) / 1e12,
                      "frac_of_peak": sum(passes.values()) / (gemm_ms * 1e-3) / 1e12 / tflops_sus,
                      "ms": {n: per[n] for n in passes}},
