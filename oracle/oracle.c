@@ -180,6 +180,31 @@ void oracle_unpermute_combine(const uint16_t* Y, const int32_t* row_id_map,
     }
 }
 
+/* Backward of the combine above ([W] unpermute_bwd: gradients of the
+ * unpermute forward, which also takes the forward's input for the
+ * probabilities' gradient; prob absent means unit weights).  With G = dL/d out:
+ *   dY[row(f)] = w[f] * G[t]                      (every slot f = t*topk + j)
+ *   dw[f]      = sum_n G[t, n] * Y[row(f), n]     (skipped when dw == NULL)
+ * Y is needed only for dw. */
+void oracle_unpermute_combine_bwd(const uint16_t* G, const uint16_t* Y, const int32_t* row_id_map,
+                                  const float* topk_w, int64_t T, int topk, int64_t N, double* dY,
+                                  double* dw) {
+    for (int64_t t = 0; t < T; ++t) {
+        for (int j = 0; j < topk; ++j) {
+            int64_t f = t * topk + j;
+            int64_t row = row_id_map ? row_id_map[f] : f;
+            double w = topk_w ? (double)topk_w[f] : 1.0;
+            double dot = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                double g = bf16_to_double(G[t * N + n]);
+                dY[row * N + n] = w * g;
+                if (dw) dot += g * bf16_to_double(Y[row * N + n]);
+            }
+            if (dw) dw[f] = dot;
+        }
+    }
+}
+
 /* ------------------------------------------------------- grouped GEMM fwd -- */
 
 /* Expert that owns expert-order row i (offsets is the exclusive prefix). */

@@ -59,6 +59,8 @@ def _load():
             "oracle_ragged_k_starts": (None, [_i32p, _int, _int, _int, _i32p]),
             "oracle_permute": (None, [_u16p, _i32p, _i64, _int, _i64, _u16p]),
             "oracle_unpermute_combine": (None, [_u16p, _vp, _vp, _i64, _int, _i64, _f64p]),
+            "oracle_unpermute_combine_bwd": (None, [_u16p, _vp, _vp, _vp, _i64, _int, _i64, _f64p,
+                                                    _vp]),
             "oracle_forward": (None, [_u16p, _u16p, _i32p, _vp, _vp, _i64, _int, _int, _i64, _i64,
                                       _int, _int, _int, _f64p]),
             "oracle_forward_rows": (None, [_u16p, _u16p, _i32p, _vp, _vp, _int, _int, _i64, _i64,
@@ -162,6 +164,20 @@ def unpermute_combine(Y, row_id_map, topk_w, T: int, topk: int) -> np.ndarray:
     out = np.empty((T, N), np.float64)
     _load().oracle_unpermute_combine(Y, _ptr(rim), _ptr(w), T, topk, N, out)
     return out
+
+
+def unpermute_combine_bwd(G, Y, row_id_map, topk_w, T: int, topk: int, want_dw: bool = True):
+    """(dY [R, N] fp64, dw [T, topk] fp64 or None) for the combine's backward."""
+    G = _c(G, np.uint16)
+    N = G.shape[1]
+    R = T * topk
+    Yc = None if (Y is None or not want_dw) else _c(Y, np.uint16)
+    rim = None if row_id_map is None else _c(row_id_map, np.int32)
+    w = None if topk_w is None else _c(topk_w, np.float32)
+    dY = np.empty((R, N), np.float64)
+    dw = np.empty((T, topk), np.float64) if want_dw else None
+    _load().oracle_unpermute_combine_bwd(G, _ptr(Yc), _ptr(rim), _ptr(w), T, topk, N, dY, _ptr(dw))
+    return dY, dw
 
 
 # ----------------------------------------------------------- grouped GEMMs --

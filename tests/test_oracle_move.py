@@ -121,3 +121,47 @@ def test_topk_sum_integer_exact():
     # brute force one entry
     t, k = 17, 9
     assert out[t, k] == sum(orc.widen_bf16(d)[t * topk + j, k] for j in range(topk))
+
+
+@pytest.mark.parametrize("topk,use_map,use_w", [(2, True, True), (4, False, True), (1, True, False),
+                                                (8, True, True)])
+def test_combine_bwd_matches_autograd(topk, use_map, use_w):
+    """The combine's backward (dY and the routing-weight gradient) equals torch
+    autograd through a dense formulation of the forward combine."""
+    import torch
+    T, E, N = 23, 6, 16
+    ids, r = _route(T, topk, E, 40 + topk)
+    rng = np.random.default_rng(topk)
+    Y = orc.round_bf16(rng.standard_normal((T * topk, N)))
+    G = orc.round_bf16(rng.standard_normal((T, N)))
+    w = rng.random((T, topk)).astype(np.float32) if use_w else None
+    rim = r["row_id_map"] if use_map else None
+    dY, dw = orc.unpermute_combine_bwd(G, Y, rim, w, T, topk)
+    Yt = torch.from_numpy(orc.widen_bf16(Y)).requires_grad_(True)
+    wt = torch.from_numpy(w.astype(np.float64) if use_w else np.ones((T, topk))).requires_grad_(True)
+    rows = torch.from_numpy((rim if use_map else np.arange(T * topk)).astype(np.int64))
+    out = (wt.reshape(-1, 1) * Yt[rows]).reshape(T, topk, N).sum(1)
+    (out * torch.from_numpy(orc.widen_bf16(G))).sum().backward()
+    np.testing.assert_allclose(dY, Yt.grad.numpy(), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(dw, wt.grad.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_combine_bwd_is_the_adjoint_of_combine_integer_exact():
+    T, topk, E, N = 31, 3, 5, 12
+    ids, r = _route(T, topk, E, 77)
+    rng = np.random.default_rng(3)
+    Y = orc.round_bf16(rng.integers(-6, 7, size=(T * topk, N)).astype(np.float64))
+    G = orc.round_bf16(rng.integers(-6, 7, size=(T, N)).astype(np.float64))
+    w = (rng.integers(1, 9, size=(T, topk)) / 8.0).astype(np.float32)  # dyadic: exact
+    fwd = orc.unpermute_combine(Y, r["row_id_map"], w, T, topk)
+    dY, dw = orc.unpermute_combine_bwd(G, Y, r["row_id_map"], w, T, topk)
+    # <combine(Y), G> == <Y, dY>, exactly on integers
+    assert (fwd * orc.widen_bf16(G)).sum() == (orc.widen_bf16(Y) * dY).sum()
+    # d<combine(Y), G>/dw[t, j] == <G[t], Y[row]>: brute force one entry
+    t, j = 13, 2
+    row = r["row_id_map"][t * topk + j]
+    assert dw[t, j] == (orc.widen_bf16(G)[t] * orc.widen_bf16(Y)[row]).sum()
+    # without Y, only dY comes back and it equals the weighted broadcast
+    dY2, dw2 = orc.unpermute_combine_bwd(G, None, r["row_id_map"], w, T, topk, want_dw=False)
+    assert dw2 is None
+    np.testing.assert_array_equal(dY2, dY)
