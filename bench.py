@@ -8,6 +8,8 @@ A step is one pass of the whole hot path over one batch of synthetic input
     GEMM1 fwd      gg_forward              Xp (dense TMA operands)
     GEMM2 fwd      gg_forward              permute_y (scatter to token order fused)
     combine        gg_unpermute_combine    weighted top-k combine -> [T, hidden]
+    combine bwd    gg_unpermute_combine_bwd  dY2 = w * G in token-slot order, and the
+                                           routing-weight gradient dw
     permute        gg_permute              dY2 (token-slot order) -> expert order
     GEMM2 bwd      gg_backward_dX, gg_backward_dW on the expert-ordered dY2
     GEMM1 bwd      gg_backward_dX (permute_x scatter store + top-k token sum),
@@ -15,8 +17,8 @@ A step is one pass of the whole hot path over one batch of synthetic input
 Materialising the expert-ordered operands once (about 0.03-0.05 ms each) lets
 every GEMM read dense TMA tiles; the fused-gather variants of the same calls
 compute the same values (tests) and are timed separately under "variants".
-The GEMM2 input stands in for act(GEMM1) (a seeded tensor), and the output
-gradients are seeded tensors; FLOPs counted are 2*R*N*K per GEMM pass (6
+The GEMM2 input stands in for act(GEMM1) (a seeded tensor); the gradient of the
+layer output G and of GEMM1's output dH are seeded tensors; FLOPs counted are 2*R*N*K per GEMM pass (6
 passes), padding rows not counted.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gg|reference]
@@ -136,7 +138,10 @@ def oracle_sample(cfg, host, ro, rows_per_pass, rng):
     orc.forward_rows(host["A2"], host["W2"], ro["m_sizes"], ro["gather_idx"], host["w"], cfg.topk,
                      0, 1, 0, rows)
     flops += rows.size * 2.0 * cfg.K * cfg.I
-    orc.backward_dX_rows(host["dY2"], host["W2"], ro["m_sizes"], ro["gather_idx"], 0, 1, rows)
+    # combine backward (the whole tensor): dY2 = w * G in token-slot order
+    dY2 = orc.round_bf16(orc.unpermute_combine_bwd(host["G"], None, None, host["w"], cfg.T, cfg.topk,
+                                                   want_dw=False)[0])
+    orc.backward_dX_rows(dY2, host["W2"], ro["m_sizes"], ro["gather_idx"], 0, 1, rows)
     flops += rows.size * 2.0 * cfg.K * cfg.I
     orc.backward_dX_rows(host["dH"], host["W1"], ro["m_sizes"], ro["gather_idx"], 1, 0, rows)
     flops += rows.size * 2.0 * cfg.N1 * cfg.K
@@ -144,14 +149,14 @@ def oracle_sample(cfg, host, ro, rows_per_pass, rng):
     es = rng.integers(0, cfg.E, size=max(1, rows_per_pass // 4)).astype(np.int32)
     es = np.array([e for e in es if ro["m_sizes"][e] > 0] or [int(np.argmax(ro["m_sizes"]))], np.int32)
     ns2 = rng.integers(0, cfg.K, size=es.size).astype(np.int64)
-    orc.backward_dW_rows(host["A2"], host["dY2"], ro["m_sizes"], ro["gather_idx"], cfg.topk, 0, 1, es, ns2)
+    orc.backward_dW_rows(host["A2"], dY2, ro["m_sizes"], ro["gather_idx"], cfg.topk, 0, 1, es, ns2)
     flops += float(sum(2.0 * ro["m_sizes"][e] * cfg.I for e in es))
     ns1 = rng.integers(0, cfg.N1, size=es.size).astype(np.int64)
     orc.backward_dW_rows(host["X"], host["dH"], ro["m_sizes"], ro["gather_idx"], cfg.topk, 1, 0, es, ns1)
     flops += float(sum(2.0 * ro["m_sizes"][e] * cfg.K for e in es))
     dt = time.perf_counter() - t0
-    desc = ("full route + %d expert-order rows of each forward and dX pass + %d rows of each dW "
-            "pass (oracle, fp64, OpenMP)" % (rows.size, es.size))
+    desc = ("full route + full combine backward + %d expert-order rows of each forward and dX "
+            "pass + %d rows of each dW pass (oracle, fp64, OpenMP)" % (rows.size, es.size))
     return dt, flops, desc
 
 
@@ -223,7 +228,7 @@ class Clocks:
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -284,7 +289,7 @@ def run_gg(args, cfg):
         return t.pin_memory()
 
     W1, W2 = to_dev(host["W1"]), to_dev(host["W2"])
-    inputs_host = {"X": host["X"], "A2": host["A2"], "dY2": host["dY2"], "dH": host["dH"]}
+    inputs_host = {"X": host["X"], "A2": host["A2"], "G": host["G"], "dH": host["dH"]}
     d = {n: to_dev(v) for n, v in inputs_host.items()}
     ids = torch.from_numpy(host["ids"]).to(dev)
     wts = torch.from_numpy(host["w"]).to(dev)
@@ -309,9 +314,11 @@ def run_gg(args, cfg):
     passes = _gemm_passes(cfg)
     step_flops = sum(passes.values())
 
-    ev_names = ["route", "permute", "fwd1", "fwd2", "combine", "permute_dY", "dX2", "dW2", "dX1",
-                "dW1"]
+    ev_names = ["route", "permute", "fwd1", "fwd2", "combine", "combine_bwd", "permute_dY", "dX2",
+                "dW2", "dX1", "dW1"]
     dYp = torch.empty(R, K, dtype=bf, device=dev)
+    dY2 = torch.empty(R, K, dtype=bf, device=dev)
+    dwt = torch.empty(T, k, dtype=torch.float32, device=dev)
 
     def step(src, evs=None):
         def mark(i):
@@ -330,24 +337,28 @@ def run_gg(args, cfg):
         mark(4)
         gg.unpermute_combine(Y2, None, src["w"], T, k, out=out, status=status)
         mark(5)
-        # dY2 arrives in token-slot order (the forward scattered with permute_y)
-        gg.permute(src["dY2"], r["row_id_map"], 1, out=dYp, status=status)
+        # backward of the combine: dY2 in token-slot order (the forward scattered
+        # with permute_y) and the routing-weight gradient
+        gg.unpermute_combine_bwd(src["G"], Y2, None, src["w"], T, k, out=dY2, out_dw=dwt,
+                                 status=status)
         mark(6)
+        gg.permute(dY2, r["row_id_map"], 1, out=dYp, status=status)
+        mark(7)
         gg.backward_dX(dYp, W2, r["m_sizes"], r["gather_idx"], T, k, False, False, out=dA2,
                        status=status)
-        mark(7)
+        mark(8)
         gg.backward_dW(src["A2"], dYp, r["m_sizes"], r["gather_idx"], T, k, False, False,
                        out=dW2, status=status)
-        mark(8)
+        mark(9)
         gg.backward_dX(src["dH"], W1, r["m_sizes"], r["gather_idx"], T, k, True, False,
                        token_sum=True, out=dX1, out_tok=dXt, status=status)
-        mark(9)
+        mark(10)
         gg.backward_dW(Xp, src["dH"], r["m_sizes"], r["gather_idx"], T, k, False, False, out=dW1,
                        status=status)
-        mark(10)
+        mark(11)
 
-    # route(4) permute fwd fwd combine permute dX dW dX(+token sum) dW
-    launches_per_step = 4 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 2 + 1
+    # route(4) permute fwd fwd combine combine-bwd permute dX dW dX(+token sum) dW
+    launches_per_step = 4 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 2 + 1
     src = dict(d, ids=ids, w=wts)
     for _ in range(max(args.warmup, 3)):
         step(src)
@@ -433,10 +444,10 @@ def run_gg(args, cfg):
             src["X"], W1, rr["m_sizes"], rr["gather_idx"], None, k, True, False, False, out=H,
             status=status)), passes["fwd1"]),
         "dX2_fused_slot_gather": (time_call(lambda: gg.backward_dX(
-            src["dY2"], W2, rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dA2,
+            dY2, W2, rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dA2,
             status=status)), passes["dX2"]),
         "dW2_fused_slot_gather": (time_call(lambda: gg.backward_dW(
-            src["A2"], src["dY2"], rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dW2,
+            src["A2"], dY2, rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dW2,
             status=status)), passes["dW2"]),
         "dW1_fused_token_gather": (time_call(lambda: gg.backward_dW(
             src["X"], src["dH"], rr["m_sizes"], rr["gather_idx"], T, k, True, False, out=dW1,
@@ -449,6 +460,8 @@ def run_gg(args, cfg):
     comb_bytes = R * K * 2 + R * 4 + T * K * 2  # weights R*4 also read
     comb_bytes += R * 4
     permdy_bytes = 2 * R * K * 2 + R * 4
+    # combine backward: read G once, write dY2, read Y2 for dw, weights, write dw
+    combbwd_bytes = T * K * 2 + R * K * 2 + R * K * 2 + R * 4 + R * 4
 
     if int(status.item()) != 0:
         raise RuntimeError("device status %d after the timed region" % int(status.item()))
@@ -477,6 +490,7 @@ def run_gg(args, cfg):
                      "ms": {n: per[n] for n in passes}},
             "hbm_movers": {"permute_GBps": perm_bytes / (per["permute"] * 1e-3) / 1e9,
                            "permute_dY_GBps": permdy_bytes / (per["permute_dY"] * 1e-3) / 1e9,
+                           "combine_bwd_GBps": combbwd_bytes / (per["combine_bwd"] * 1e-3) / 1e9,
                            "combine_GBps": comb_bytes / (per["combine"] * 1e-3) / 1e9,
                            "peak_GBps": hbm, "peak_source": src_kind,
                            "permute_frac": perm_bytes / (per["permute"] * 1e-3) / 1e9 / hbm,
@@ -505,7 +519,7 @@ def run_gg(args, cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gg", choices=["gg", "reference"])
     ap.add_argument("--config", default="mlp8")

@@ -149,6 +149,21 @@ int gg_unpermute_combine(const gg_bf16* Y, const int32_t* row_id_map, const floa
                          int64_t T, int topk, int64_t N, gg_bf16* out, int32_t* status,
                          void* stream);
 
+/* ----------------------------------------------- unpermute-combine, bwd --
+ * Gradient of gg_unpermute_combine ([W] unpermute_bwd: gradients of the
+ * unpermute forward, taking the forward's input for the probabilities'
+ * gradient; no probabilities means unit weights).  With G = dL/d out:
+ *   dY[row(f), :] = bf16( w[f] * G[t, :] )            for every slot f = t*topk + j
+ *   dw[f]         = sum_n G[t, n] * Y[row(f), n]      (fp32)
+ *  G [T, N] bf16; Y [R, N] bf16, the forward's input (needed only for dw);
+ *  row_id_map [R] int32 or NULL (identity); topk_w [T, topk] fp32 or NULL (1);
+ *  dY [R, N] bf16 out (every row written once); dw [T, topk] fp32 out or NULL.
+ *  dw without Y -> GG_ERR_INVALID_ARG.  Deterministic (fixed reduction order).
+ *  A map entry outside [0, R) sets GG_DEV_BAD_ROW_INDEX; that slot gets dw 0. */
+int gg_unpermute_combine_bwd(const gg_bf16* G, const gg_bf16* Y, const int32_t* row_id_map,
+                             const float* topk_w, int64_t T, int topk, int64_t N, gg_bf16* dY,
+                             float* dw, int32_t* status, void* stream);
+
 /* ---------------------------------------------------------------- forward --
  * Grouped GEMM forward ([U] grouped_gemm_forward; [V] matmul_ogs docstring:
  * Y[idx_y(e)] = X[idx_x(e)] @ W[e]^T):

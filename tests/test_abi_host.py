@@ -80,6 +80,10 @@ def test_host_validation_codes(lib):
     assert L.gg_dual_asym(None, None, None, None, None, None, 0, 0, 8, 8, 8, 0, 0, None, None) == _lib.GG_OK
     # dual sizes must be multiples of 8
     assert L.gg_dual_asym(fake, fake, fake, fake, fake, fake, 12, 8, 8, 8, 8, 0, 0, None, None) == _lib.GG_ERR_UNSUPPORTED
+    # combine backward: dw needs the forward input; empty problems launch nothing
+    assert L.gg_unpermute_combine_bwd(fake, None, None, None, 4, 2, 8, fake, fake, None, None) == _lib.GG_ERR_INVALID_ARG
+    assert L.gg_unpermute_combine_bwd(fake, fake, None, None, 4, 2, 12, fake, None, None, None) == _lib.GG_ERR_UNSUPPORTED
+    assert L.gg_unpermute_combine_bwd(None, None, None, None, 0, 2, 8, None, None, None, None) == _lib.GG_OK
     # route: workspace too small, bad sizes
     ws = L.gg_route_workspace_size(64, 2, 4)
     assert L.gg_route_hist_offsets(fake, 64, 2, 4, 0, fake, fake, None, fake, fake, fake, ws - 1, None, None) == _lib.GG_ERR_WORKSPACE

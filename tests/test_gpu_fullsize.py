@@ -71,14 +71,16 @@ def _run_layer(cfg):
     res["dX1"], res["dXt"] = hbf(dX1), hbf(dXt)
     res["dW1"] = hbf(gg.backward_dW(Xp, dH, r["m_sizes"], r["gather_idx"], T, k, status=st))
     if I:
-        A2, W2, dY2 = dbf(host["A2"]), dbf(host["W2"]), dbf(host["dY2"])
+        A2, W2, G = dbf(host["A2"]), dbf(host["W2"]), dbf(host["G"])
         wt = df32(w)
         Y2 = gg.forward(A2, W2, r["m_sizes"], r["gather_idx"], None, k, False, True, status=st)
         res["Y2"] = hbf(Y2)
         res["out"] = hbf(gg.unpermute_combine(Y2, None, wt, T, k, status=st))
+        dY2, dw = gg.unpermute_combine_bwd(G, Y2, None, wt, T, k, status=st)
+        res["dY2"], res["dw"] = hbf(dY2), dw.cpu().numpy().astype(np.float64)
         res["Y2_scaled"] = hbf(gg.forward(A2, W2, r["m_sizes"], r["gather_idx"], wt, k, False, True,
                                           True, status=st))
-        dYp = gg.permute(dY2, r["row_id_map"], 1, status=st)
+        dYp = gg.permute(dY2, r["row_id_map"], 1, status=st)  # token-slot -> expert order
         res["dA2"] = hbf(gg.backward_dX(dYp, W2, r["m_sizes"], r["gather_idx"], T, k, status=st))
         res["dA2_fused"] = hbf(gg.backward_dX(dY2, W2, r["m_sizes"], r["gather_idx"], T, k, False, True,
                                               status=st))
@@ -144,12 +146,23 @@ def test_full_layer_sampled(name):
         ref = orc.unpermute_combine(ysub, None, w[toks], toks.size, k)
         mag = (np.abs(orc.widen_bf16(ysub)).reshape(toks.size, k, K) * w[toks][:, :, None]).sum(axis=1)
         assert_close(res["out"][toks], ref, name + " combine", magnitude=mag)
+        # combine backward: dY2 in full, dw of the sampled tokens from oracle rows
+        rdY2 = orc.unpermute_combine_bwd(host["G"], None, None, w, T, k, want_dw=False)[0]
+        assert_close(res["dY2"], rdY2, name + " combine bwd dY2")
+        dY2h = orc.round_bf16(rdY2)
+        _, rdw = orc.unpermute_combine_bwd(host["G"][toks], ysub, None, None, toks.size, k)
+        # each forward row element may sit one bf16 step (<= 2^-7 of itself) from the oracle's
+        Ga, Ya = np.abs(orc.widen_bf16(host["G"][toks])), np.abs(orc.widen_bf16(ysub)).reshape(toks.size, k, K)
+        bound = 2.0 ** -7 * np.einsum("tn,tjn->tj", Ga, Ya) + 1e-6
+        d = res["dw"][toks] - rdw
+        assert (np.abs(d) <= bound).all(), name + " dw elementwise"
+        assert np.linalg.norm(d) <= 1e-2 * np.linalg.norm(rdw), name + " dw rel-Frobenius"
         # GEMM2 backward on the expert-ordered dY2, and with the slot gather fused
-        vals, dest = orc.backward_dX_rows(host["dY2"], host["W2"], m, g, 0, 1, rows)
+        vals, dest = orc.backward_dX_rows(dY2h, host["W2"], m, g, 0, 1, rows)
         assert_close(res["dA2"][dest], vals, name + " dX2")
         assert_close(res["dA2_fused"][dest], vals, name + " dX2 (fused gather)")
         es, ns, empty = _sample_dw(m, K, rng)
-        vals = orc.backward_dW_rows(host["A2"], host["dY2"], m, g, k, 0, 1, es, ns)
+        vals = orc.backward_dW_rows(host["A2"], dY2h, m, g, k, 0, 1, es, ns)
         assert_close(res["dW2"][es, ns], vals, name + " dW2")
         for e in empty:
             assert (res["dW2"][e] == 0).all()
@@ -168,8 +181,9 @@ def test_tiny_full():
     assert_close(res["Y2_scaled"], orc.forward(host["A2"], host["W2"], m, g, w, T, k, 0, 1, 1), "tiny fwd2")
     assert_close(res["dX1"], orc.backward_dX(host["dH"], host["W1"], m, g, T, k, 1, 0), "tiny dX1")
     assert_close(res["dW1"], orc.backward_dW(host["X"], host["dH"], m, g, T, k, 1, 0), "tiny dW1")
-    assert_close(res["dA2"], orc.backward_dX(host["dY2"], host["W2"], m, g, T, k, 0, 1), "tiny dX2")
-    assert_close(res["dW2"], orc.backward_dW(host["A2"], host["dY2"], m, g, T, k, 0, 1), "tiny dW2")
+    dY2h = orc.round_bf16(orc.unpermute_combine_bwd(host["G"], None, None, w, T, k, want_dw=False)[0])
+    assert_close(res["dA2"], orc.backward_dX(dY2h, host["W2"], m, g, T, k, 0, 1), "tiny dX2")
+    assert_close(res["dW2"], orc.backward_dW(host["A2"], dY2h, m, g, T, k, 0, 1), "tiny dW2")
 
 
 @pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])

@@ -116,6 +116,34 @@ def test_unpermute_combine(T, topk, N, use_map, use_w):
     np.testing.assert_array_equal(np.abs(orc.widen_bf16(hbf(out)) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30, True)
 
 
+@pytest.mark.parametrize("T,topk,N,use_map,use_w,want_dw", [
+    (64, 2, 256, True, True, True), (300, 8, 40, True, False, True), (129, 4, 1032, False, True, True),
+    (50, 1, 8, False, False, False), (77, 3, 264, True, True, False)])
+def test_unpermute_combine_bwd(T, topk, N, use_map, use_w, want_dw):
+    E = 5
+    ids = _ids(T, topk, E, N + 1)
+    ro = orc.route(ids, T, topk, E)
+    rng = np.random.default_rng(N + 1)
+    G = synth.normal_bf16(N, "cg", (T, N), 0.25)
+    Y = synth.normal_bf16(N, "cyb", (T * topk, N), 0.25)
+    w = rng.random((T, topk)).astype(np.float32) if use_w else None
+    rim = ro["row_id_map"] if use_map else None
+    st = status_tensor()
+    dY, dw = gg.unpermute_combine_bwd(dbf(G), dbf(Y) if want_dw else None,
+                                      None if rim is None else di32(rim),
+                                      None if w is None else df32(w), T, topk, want_dw=want_dw,
+                                      status=st)
+    assert status_of(st) == 0
+    rdY, rdw = orc.unpermute_combine_bwd(G, Y, rim, w, T, topk, want_dw=want_dw)
+    assert_close(hbf(dY), rdY, "combine bwd dY")
+    if want_dw:
+        got = dw.cpu().numpy().astype(np.float64)
+        scale = float(np.sqrt(np.mean(rdw * rdw))) + 1e-30
+        assert np.abs(got - rdw).max() <= 1e-4 * scale + 1e-6 * np.abs(rdw).max(), "combine bwd dw"
+    else:
+        assert dw is None
+
+
 # ---------------------------------------------------------- grouped GEMMs --
 
 SHAPES = [

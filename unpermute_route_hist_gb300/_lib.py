@@ -31,6 +31,7 @@ SIGNATURES = {
                                              _vp, _vp]),
     "gg_permute": (_int, [_vp, _vp, _i64, _int, _i64, _vp, _vp, _vp]),
     "gg_unpermute_combine": (_int, [_vp, _vp, _vp, _i64, _int, _i64, _vp, _vp, _vp]),
+    "gg_unpermute_combine_bwd": (_int, [_vp, _vp, _vp, _vp, _i64, _int, _i64, _vp, _vp, _vp, _vp]),
     "gg_forward": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _int, _int,
                           _vp, _vp, _vp]),
     "gg_backward_dX": (_int, [_vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _int, _vp, _vp,

@@ -98,6 +98,27 @@ def unpermute_combine(Y, row_id_map, topk_w, T: int, topk: int, *, out=None, sta
     return o
 
 
+def unpermute_combine_bwd(G, Y, row_id_map, topk_w, T: int, topk: int, *, want_dw=True, out=None,
+                          out_dw=None, status=None):
+    """(dY [T*topk, N] bf16, dw [T, topk] fp32 or None): the combine's backward."""
+    _need(G, torch.bfloat16, "G", (T, G.shape[1]))
+    N = G.shape[1]
+    R = T * topk
+    if want_dw:
+        _need(Y, torch.bfloat16, "Y", (R, N))
+    _opt(row_id_map, torch.int32, "row_id_map", (R,))
+    _opt(topk_w, torch.float32, "topk_w")
+    if topk_w is not None and topk_w.numel() != R:
+        raise ValueError("topk_w must have T*topk elements")
+    dY = _out(out, (R, N), torch.bfloat16, G.device, "out")
+    dw = _out(out_dw, (T, topk), torch.float32, G.device, "out_dw") if want_dw else None
+    rc = _lib.load().gg_unpermute_combine_bwd(_p(G), _p(Y) if want_dw else None, _p(row_id_map),
+                                              _p(topk_w), T, topk, N, _p(dY), _p(dw), _p(status),
+                                              _stream(G.device))
+    _lib.check("gg_unpermute_combine_bwd", rc)
+    return dY, dw
+
+
 def forward(X, W, m_sizes, gather_idx, topk_w, topk: int, permute_x=False, permute_y=False,
             fuse_mul_post=False, *, out=None, status=None):
     _need(X, torch.bfloat16, "X")

@@ -20,6 +20,9 @@ int permute_launch(const uint16_t* X, const int32_t* row_id_map, int64_t T, int 
                    uint16_t* Xp, int32_t* status, cudaStream_t stream);
 int combine_launch(const uint16_t* Y, const int32_t* row_id_map, const float* topk_w, int64_t T,
                    int topk, int64_t N, uint16_t* out, int32_t* status, cudaStream_t stream);
+int combine_bwd_launch(const uint16_t* G, const uint16_t* Y, const int32_t* row_id_map,
+                       const float* topk_w, int64_t T, int topk, int64_t N, uint16_t* dY, float* dw,
+                       int32_t* status, cudaStream_t stream);
 
 namespace {
 thread_local char g_last_error[256] = "no error";
@@ -199,6 +202,27 @@ int gg_unpermute_combine(const gg_bf16* Y, const int32_t* row_id_map, const floa
     if (!al16(Y) || !al16(out)) return GG_ERR_UNSUPPORTED;
     return check_launch(
         combine_launch(Y, row_id_map, topk_w, T, topk, N, out, status, as_stream(stream)));
+}
+
+int gg_unpermute_combine_bwd(const gg_bf16* G, const gg_bf16* Y, const int32_t* row_id_map,
+                             const float* topk_w, int64_t T, int topk, int64_t N, gg_bf16* dY,
+                             float* dw, int32_t* status, void* stream) {
+    if (T < 0 || topk < 1 || N < 0) return GG_ERR_INVALID_ARG;
+    if (topk > GG_MAX_TOPK || N % 8) return GG_ERR_UNSUPPORTED;
+    if (T * topk >= (int64_t(1) << 31)) return GG_ERR_UNSUPPORTED;
+    if (T == 0) return GG_OK;
+    if (dw && !Y && N > 0) return GG_ERR_INVALID_ARG;
+    if (N == 0) {
+        if (!dw) return GG_OK;
+        const cudaError_t e = cudaMemsetAsync(dw, 0, sizeof(float) * static_cast<size_t>(T * topk),
+                                              as_stream(stream));
+        if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+        return GG_OK;
+    }
+    if (!G || !dY) return GG_ERR_INVALID_ARG;
+    if (!al16(G) || !al16(dY) || (Y && !al16(Y))) return GG_ERR_UNSUPPORTED;
+    return check_launch(combine_bwd_launch(G, dw ? Y : nullptr, row_id_map, topk_w, T, topk, N, dY,
+                                           dw, status, as_stream(stream)));
 }
 
 int gg_selftest_bounded_wait(int32_t* status, int32_t* result, uint64_t limit_ns, void* stream) {

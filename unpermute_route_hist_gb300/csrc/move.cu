@@ -8,6 +8,9 @@
 //                     over a token's slots (backend.py, unpermute; matmul_ogs.py,
 //                     matmul_ogs_torch's fp32 accumulation).  Output-stationary
 //                     and deterministic: out[t] sums its slots in slot order.
+//  combine backward   its gradient (backend.py, unpermute_bwd): each slot's row
+//                     gets the token's output gradient times the slot weight,
+//                     and each weight gets <output gradient, forward row>.
 //
 // Both move whole rows as 16-byte vectors (row widths are multiples of 8
 // bf16), one CTA per row in a grid that is a multiple of the SM count.
@@ -97,6 +100,84 @@ combine_kernel(const uint4* __restrict__ Y, const int32_t* __restrict__ row_id_m
     }
 }
 
+// Backward of the combine: dY[row(f)] = bf16(w[f] * G[t]); dw[f] = <G[t], Y[row(f)]>.
+// One CTA per token; G[t] is read from HBM once (its chunks stay in L1 across the
+// token's slots); each slot's dot product is summed per thread, then per warp
+// (shuffle tree), then over warps in warp order, so the result is deterministic.
+__global__ void __launch_bounds__(kMoveThreads)
+combine_bwd_kernel(const uint4* __restrict__ G, const uint4* __restrict__ Y,
+                   const int32_t* __restrict__ row_id_map, const float* __restrict__ topk_w,
+                   int64_t T, int topk, int64_t row_vecs, int64_t R, uint4* __restrict__ dY,
+                   float* __restrict__ dw, int32_t* status) {
+    constexpr int kWarps = kMoveThreads / 32;
+    __shared__ int32_t row_s[GG_MAX_TOPK];
+    __shared__ float w_s[GG_MAX_TOPK];
+    __shared__ float part_s[kWarps][GG_MAX_TOPK];
+    const int lane = lane_id(), warp = warp_id();
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        __syncthreads();
+        if (threadIdx.x < topk) {
+            const int64_t f = t * topk + threadIdx.x;
+            int32_t r = row_id_map ? row_id_map[f] : static_cast<int32_t>(f);
+            if (r < 0 || r >= R) {
+                set_status(status, GG_DEV_BAD_ROW_INDEX);
+                r = -1;
+            }
+            row_s[threadIdx.x] = r;
+            w_s[threadIdx.x] = topk_w ? topk_w[f] : 1.0f;
+        }
+        __syncthreads();
+        const uint4* g_row = G + t * row_vecs;
+        for (int j = 0; j < topk; ++j) {
+            const int32_t r = row_s[j];
+            const float w = w_s[j];
+            float dot = 0.f;
+            for (int64_t c = threadIdx.x; c < row_vecs; c += kMoveThreads) {
+                const uint4 gv = __ldg(g_row + c);
+                const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&gv);
+                float gf[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f2 = __bfloat1622float2(gh[q]);
+                    gf[2 * q] = f2.x;
+                    gf[2 * q + 1] = f2.y;
+                }
+                if (r >= 0) {
+                    uint4 o;
+                    o.x = pack_bf16x2(w * gf[0], w * gf[1]);
+                    o.y = pack_bf16x2(w * gf[2], w * gf[3]);
+                    o.z = pack_bf16x2(w * gf[4], w * gf[5]);
+                    o.w = pack_bf16x2(w * gf[6], w * gf[7]);
+                    dY[static_cast<int64_t>(r) * row_vecs + c] = o;
+                    if (dw) {
+                        const uint4 yv = ld_stream(Y + static_cast<int64_t>(r) * row_vecs + c);
+                        const __nv_bfloat162* yh = reinterpret_cast<const __nv_bfloat162*>(&yv);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 y2 = __bfloat1622float2(yh[q]);
+                            dot = fmaf(gf[2 * q], y2.x, dot);
+                            dot = fmaf(gf[2 * q + 1], y2.y, dot);
+                        }
+                    }
+                }
+            }
+            if (dw) {
+#pragma unroll
+                for (int d = 16; d > 0; d >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, d);
+                if (lane == 0) part_s[warp][j] = dot;
+            }
+        }
+        if (dw) {
+            __syncthreads();
+            if (threadIdx.x < topk) {
+                float sum = 0.f;
+                for (int q = 0; q < kWarps; ++q) sum += part_s[q][threadIdx.x];
+                dw[t * topk + threadIdx.x] = row_s[threadIdx.x] >= 0 ? sum : 0.f;
+            }
+        }
+    }
+}
+
 unsigned move_grid(int64_t rows) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -113,6 +194,16 @@ int permute_launch(const uint16_t* X, const int32_t* row_id_map, int64_t T, int 
     permute_kernel<<<move_grid(T), kMoveThreads, 0, stream>>>(
         reinterpret_cast<const uint4*>(X), row_id_map, T, topk, K / 8, reinterpret_cast<uint4*>(Xp),
         R, status);
+    return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
+}
+
+int combine_bwd_launch(const uint16_t* G, const uint16_t* Y, const int32_t* row_id_map,
+                       const float* topk_w, int64_t T, int topk, int64_t N, uint16_t* dY, float* dw,
+                       int32_t* status, cudaStream_t stream) {
+    const int64_t R = T * topk;
+    combine_bwd_kernel<<<move_grid(T), kMoveThreads, 0, stream>>>(
+        reinterpret_cast<const uint4*>(G), reinterpret_cast<const uint4*>(Y), row_id_map, topk_w, T,
+        topk, N / 8, R, reinterpret_cast<uint4*>(dY), dw, status);
     return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
 }
 

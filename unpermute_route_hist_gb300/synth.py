@@ -160,13 +160,14 @@ def route_choices(cfg: MoEConfig):
     return topk_softmax_route(logits, cfg.topk)
 
 
-def moe_tensors(cfg: MoEConfig, which=("X", "W1", "W2", "A2", "dY2", "dH")) -> dict:
+def moe_tensors(cfg: MoEConfig, which=("X", "W1", "W2", "A2", "G", "dH")) -> dict:
     """Seeded bf16 tensors of a config (uint16 bits):
       X   [T, K]        token hidden states
       W1  [E, N1, K]    GEMM1 weights (E, N, K), K contiguous
       W2  [E, K, I]     GEMM2 weights
       A2  [R, I]        GEMM2 input in expert order (stands in for act(GEMM1))
-      dY2 [R, K]        gradient of GEMM2's token-major output
+      G   [T, K]        gradient of the layer output (after the top-k combine)
+      dY2 [R, K]        gradient of GEMM2's token-major output (on request)
       dH  [R, N1]       gradient of GEMM1's expert-order output
     Backward gradients use the same std (keeps dW magnitudes O(0.1))."""
     out = {}
@@ -177,6 +178,7 @@ def moe_tensors(cfg: MoEConfig, which=("X", "W1", "W2", "A2", "dY2", "dH")) -> d
         "W2": (c.E, c.K, c.I) if c.I else None,
         "A2": (c.R, c.I) if c.I else None,
         "dY2": (c.R, c.K) if c.I else None,
+        "G": (c.T, c.K) if c.I else None,
         "dH": (c.R, c.N1),
     }
     for name in which:
