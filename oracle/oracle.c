@@ -280,6 +280,38 @@ void oracle_forward_rows(const uint16_t* X, const uint16_t* W, const int32_t* m_
     free(offsets);
 }
 
+/* ---------------------------------------------------------------- SwiGLU -- */
+
+/* Gated activation over interleaved gate/up columns ([V] FusedActivation with
+ * reduction_n = 2: the activation reduces each pair of adjacent output columns
+ * to one).  h is [rows, 2*I] (fp64, e.g. a forward's exact output), act is
+ * [rows, I]:  act[r, c] = silu(g) * u,  g = h[r, 2c], u = h[r, 2c + 1],
+ * silu(g) = g / (1 + exp(-g)). */
+void oracle_swiglu(const double* h, int64_t rows, int64_t I, double* act) {
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < I; ++c) {
+            double g = h[r * 2 * I + 2 * c], u = h[r * 2 * I + 2 * c + 1];
+            act[r * I + c] = g / (1.0 + exp(-g)) * u;
+        }
+}
+
+/* Its gradient: given the stored bf16 H [rows, 2I] and dA = dL/d act [rows, I],
+ *   d gate = dA * u * s * (1 + g * (1 - s)),   s = 1 / (1 + exp(-g))
+ *   d up   = dA * g * s
+ * written interleaved into dH [rows, 2I]. */
+void oracle_swiglu_bwd(const uint16_t* H, const uint16_t* dA, int64_t rows, int64_t I,
+                       double* dH) {
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < I; ++c) {
+            double g = bf16_to_double(H[r * 2 * I + 2 * c]);
+            double u = bf16_to_double(H[r * 2 * I + 2 * c + 1]);
+            double d = bf16_to_double(dA[r * I + c]);
+            double s = 1.0 / (1.0 + exp(-g));
+            dH[r * 2 * I + 2 * c] = d * u * s * (1.0 + g * (1.0 - s));
+            dH[r * 2 * I + 2 * c + 1] = d * g * s;
+        }
+}
+
 /* ------------------------------------------------------------ backward dX -- */
 
 /* One row of dX ([U] grouped_gemm_dX): reduce over N,

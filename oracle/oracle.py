@@ -61,6 +61,8 @@ def _load():
             "oracle_unpermute_combine": (None, [_u16p, _vp, _vp, _i64, _int, _i64, _f64p]),
             "oracle_unpermute_combine_bwd": (None, [_u16p, _vp, _vp, _vp, _i64, _int, _i64, _f64p,
                                                     _vp]),
+            "oracle_swiglu": (None, [_f64p, _i64, _i64, _f64p]),
+            "oracle_swiglu_bwd": (None, [_u16p, _u16p, _i64, _i64, _f64p]),
             "oracle_forward": (None, [_u16p, _u16p, _i32p, _vp, _vp, _i64, _int, _int, _i64, _i64,
                                       _int, _int, _int, _f64p]),
             "oracle_forward_rows": (None, [_u16p, _u16p, _i32p, _vp, _vp, _int, _int, _i64, _i64,
@@ -178,6 +180,27 @@ def unpermute_combine_bwd(G, Y, row_id_map, topk_w, T: int, topk: int, want_dw: 
     dw = np.empty((T, topk), np.float64) if want_dw else None
     _load().oracle_unpermute_combine_bwd(G, _ptr(Yc), _ptr(rim), _ptr(w), T, topk, N, dY, _ptr(dw))
     return dY, dw
+
+
+def swiglu(h) -> np.ndarray:
+    """act [rows, I] from interleaved gate/up columns h [rows, 2I] (fp64)."""
+    h = _c(h, np.float64)
+    rows, two_i = h.shape
+    assert two_i % 2 == 0
+    act = np.empty((rows, two_i // 2), np.float64)
+    _load().oracle_swiglu(h, rows, two_i // 2, act)
+    return act
+
+
+def swiglu_bwd(H, dA) -> np.ndarray:
+    """dH [rows, 2I] (fp64) from the stored bf16 H [rows, 2I] and dA [rows, I]."""
+    H = _c(H, np.uint16)
+    dA = _c(dA, np.uint16)
+    rows, two_i = H.shape
+    assert dA.shape == (rows, two_i // 2)
+    dH = np.empty((rows, two_i), np.float64)
+    _load().oracle_swiglu_bwd(H, dA, rows, two_i // 2, dH)
+    return dH
 
 
 # ----------------------------------------------------------- grouped GEMMs --

@@ -209,3 +209,28 @@ def test_sampled_rows_agree_with_full():
     Y0, Y1 = orc.dual_asym(d["X0"], d["X1"], d["W0"], d["W1"], True, False)
     np.testing.assert_array_equal(orc.dual_asym_rows(d["X1"], d["W1"], 8, 16, 8, True, False,
                                                      np.array([7, 0, 3])), Y1[[7, 0, 3]])
+
+
+def test_swiglu_matches_library_silu_and_closed_forms():
+    rng = np.random.default_rng(8)
+    h = rng.standard_normal((37, 2 * 24)) * 3
+    act = orc.swiglu(h)
+    g, u = h[:, 0::2], h[:, 1::2]
+    ref = torch.nn.functional.silu(torch.from_numpy(g)).numpy() * u
+    np.testing.assert_allclose(act, ref, rtol=1e-13, atol=1e-15)
+    # closed forms: silu(0) = 0, silu(large) -> g, silu(very negative) -> 0, u = 0 -> 0
+    hh = np.array([[0.0, 5.0, 50.0, 2.0, -60.0, 3.0, 1.5, 0.0]])
+    a = orc.swiglu(hh)[0]
+    assert a[0] == 0.0 and abs(a[1] - 100.0) < 1e-12 and abs(a[2]) < 1e-20 and a[3] == 0.0
+
+
+def test_swiglu_bwd_matches_autograd():
+    rng = np.random.default_rng(9)
+    rows, I = 29, 20
+    H = orc.round_bf16(rng.standard_normal((rows, 2 * I)) * 2)
+    dA = orc.round_bf16(rng.standard_normal((rows, I)))
+    dH = orc.swiglu_bwd(H, dA)
+    Ht = torch.from_numpy(orc.widen_bf16(H)).requires_grad_(True)
+    act = torch.nn.functional.silu(Ht[:, 0::2]) * Ht[:, 1::2]
+    (act * torch.from_numpy(orc.widen_bf16(dA))).sum().backward()
+    np.testing.assert_allclose(dH, Ht.grad.numpy(), rtol=1e-12, atol=1e-13)
