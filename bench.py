@@ -5,20 +5,22 @@ A step is one pass of the whole hot path over one batch of synthetic input
 (gate_up N = 28672), E=8 experts, top-2):
     route          gg_route_hist_offsets   histogram, offsets, stable permutation
     permute        gg_permute              X -> expert order (Xp)
-    GEMM1 fwd      gg_forward              Xp (dense TMA operands)
-    GEMM2 fwd      gg_forward              permute_y (scatter to token order fused)
+    GEMM1 fwd      gg_forward_swiglu       Xp (dense TMA operands) -> H, and the fused
+                                           SwiGLU A = silu(gate) * up (interleaved columns)
+    GEMM2 fwd      gg_forward              A, permute_y (scatter to token order fused)
     combine        gg_unpermute_combine    weighted top-k combine -> [T, hidden]
     combine bwd    gg_unpermute_combine_bwd  dY2 = w * G in token-slot order, and the
                                            routing-weight gradient dw
     permute        gg_permute              dY2 (token-slot order) -> expert order
-    GEMM2 bwd      gg_backward_dX, gg_backward_dW on the expert-ordered dY2
+    GEMM2 bwd      gg_backward_dX -> dA, gg_backward_dW on the expert-ordered dY2
+    SwiGLU bwd     gg_swiglu_bwd           dH from H and dA
     GEMM1 bwd      gg_backward_dX (permute_x scatter store + top-k token sum),
                    gg_backward_dW on Xp
 Materialising the expert-ordered operands once (about 0.03-0.05 ms each) lets
 every GEMM read dense TMA tiles; the fused-gather variants of the same calls
 compute the same values (tests) and are timed separately under "variants".
-The GEMM2 input stands in for act(GEMM1) (a seeded tensor); the gradient of the
-layer output G and of GEMM1's output dH are seeded tensors; FLOPs counted are 2*R*N*K per GEMM pass (6
+The seeded inputs are the tokens X, the layer-output gradient G, the weights
+and the router's choices; every other tensor is computed in the step; FLOPs counted are 2*R*N*K per GEMM pass (6
 passes), padding rows not counted.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gg|reference]
@@ -156,16 +158,25 @@ def oracle_sample(cfg, host, ro, rows_per_pass, rng):
     flops += float(sum(2.0 * ro["m_sizes"][e] * cfg.K for e in es))
     dt = time.perf_counter() - t0
     desc = ("full route + full combine backward + %d expert-order rows of each forward and dX "
-            "pass + %d rows of each dW pass (oracle, fp64, OpenMP)" % (rows.size, es.size))
+            "pass + %d rows of each dW pass, GEMM2 input and GEMM1 output gradient seeded "
+            "(oracle, fp64, OpenMP)" % (rows.size, es.size))
     return dt, flops, desc
 
 
-def make_host(cfg):
+def make_host(cfg, which=("X", "W1", "W2", "G")):
     from unpermute_route_hist_gb300 import synth
     ids, w = synth.route_choices(cfg)
-    host = synth.moe_tensors(cfg)
+    host = synth.moe_tensors(cfg, which)
     host["ids"], host["w"] = ids, w
     return host
+
+
+def add_oracle_operands(cfg, host):
+    """Seeded stand-ins for the GEMM2 input and GEMM1's output gradient, so the
+    oracle's row sample does not have to compute every row of the chain that
+    produces them on the GPU (same shapes, so the same work per row)."""
+    from unpermute_route_hist_gb300 import synth
+    host.update(synth.moe_tensors(cfg, ("A2", "dH")))
 
 
 def run_reference(args, cfg):
@@ -176,6 +187,7 @@ def run_reference(args, cfg):
     from oracle import oracle as orc
     orc.build()
     host = make_host(cfg)
+    add_oracle_operands(cfg, host)
     ro = orc.route(host["ids"], cfg.T, cfg.topk, cfg.E)
     rng = np.random.default_rng(1234)
     rows = args.ref_rows
@@ -289,7 +301,7 @@ def run_gg(args, cfg):
         return t.pin_memory()
 
     W1, W2 = to_dev(host["W1"]), to_dev(host["W2"])
-    inputs_host = {"X": host["X"], "A2": host["A2"], "G": host["G"], "dH": host["dH"]}
+    inputs_host = {"X": host["X"], "G": host["G"]}
     d = {n: to_dev(v) for n, v in inputs_host.items()}
     ids = torch.from_numpy(host["ids"]).to(dev)
     wts = torch.from_numpy(host["w"]).to(dev)
@@ -315,7 +327,9 @@ def run_gg(args, cfg):
     step_flops = sum(passes.values())
 
     ev_names = ["route", "permute", "fwd1", "fwd2", "combine", "combine_bwd", "permute_dY", "dX2",
-                "dW2", "dX1", "dW1"]
+                "dW2", "swiglu_bwd", "dX1", "dW1"]
+    A2 = torch.empty(R, I, dtype=bf, device=dev)
+    dH = torch.empty(R, N1, dtype=bf, device=dev)
     dYp = torch.empty(R, K, dtype=bf, device=dev)
     dY2 = torch.empty(R, K, dtype=bf, device=dev)
     dwt = torch.empty(T, k, dtype=torch.float32, device=dev)
@@ -329,10 +343,10 @@ def run_gg(args, cfg):
         mark(1)
         gg.permute(src["X"], r["row_id_map"], k, out=Xp, status=status)
         mark(2)
-        gg.forward(Xp, W1, r["m_sizes"], r["gather_idx"], None, k, False, False, False, out=H,
-                   status=status)
+        gg.forward_swiglu(Xp, W1, r["m_sizes"], r["gather_idx"], k, False, out=H, out_act=A2,
+                          status=status)
         mark(3)
-        gg.forward(src["A2"], W2, r["m_sizes"], r["gather_idx"], None, k, False, True, False, out=Y2,
+        gg.forward(A2, W2, r["m_sizes"], r["gather_idx"], None, k, False, True, False, out=Y2,
                    status=status)
         mark(4)
         gg.unpermute_combine(Y2, None, src["w"], T, k, out=out, status=status)
@@ -347,18 +361,20 @@ def run_gg(args, cfg):
         gg.backward_dX(dYp, W2, r["m_sizes"], r["gather_idx"], T, k, False, False, out=dA2,
                        status=status)
         mark(8)
-        gg.backward_dW(src["A2"], dYp, r["m_sizes"], r["gather_idx"], T, k, False, False,
+        gg.backward_dW(A2, dYp, r["m_sizes"], r["gather_idx"], T, k, False, False,
                        out=dW2, status=status)
         mark(9)
-        gg.backward_dX(src["dH"], W1, r["m_sizes"], r["gather_idx"], T, k, True, False,
-                       token_sum=True, out=dX1, out_tok=dXt, status=status)
+        gg.swiglu_bwd(H, dA2, out=dH)
         mark(10)
-        gg.backward_dW(Xp, src["dH"], r["m_sizes"], r["gather_idx"], T, k, False, False, out=dW1,
-                       status=status)
+        gg.backward_dX(dH, W1, r["m_sizes"], r["gather_idx"], T, k, True, False,
+                       token_sum=True, out=dX1, out_tok=dXt, status=status)
         mark(11)
+        gg.backward_dW(Xp, dH, r["m_sizes"], r["gather_idx"], T, k, False, False, out=dW1,
+                       status=status)
+        mark(12)
 
-    # route(4) permute fwd fwd combine combine-bwd permute dX dW dX(+token sum) dW
-    launches_per_step = 4 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 2 + 1
+    # route(4) permute fwd fwd combine combine-bwd permute dX dW swiglu-bwd dX(+token sum) dW
+    launches_per_step = 4 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 1 + 2 + 1
     src = dict(d, ids=ids, w=wts)
     for _ in range(max(args.warmup, 3)):
         step(src)
@@ -447,10 +463,10 @@ def run_gg(args, cfg):
             dY2, W2, rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dA2,
             status=status)), passes["dX2"]),
         "dW2_fused_slot_gather": (time_call(lambda: gg.backward_dW(
-            src["A2"], dY2, rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dW2,
+            A2, dY2, rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dW2,
             status=status)), passes["dW2"]),
         "dW1_fused_token_gather": (time_call(lambda: gg.backward_dW(
-            src["X"], src["dH"], rr["m_sizes"], rr["gather_idx"], T, k, True, False, out=dW1,
+            src["X"], dH, rr["m_sizes"], rr["gather_idx"], T, k, True, False, out=dW1,
             status=status), reps=1), passes["dW1"]),
     }
     variants = {n: {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12} for n, (ms, fl) in variants.items()}
@@ -462,6 +478,7 @@ def run_gg(args, cfg):
     permdy_bytes = 2 * R * K * 2 + R * 4
     # combine backward: read G once, write dY2, read Y2 for dw, weights, write dw
     combbwd_bytes = T * K * 2 + R * K * 2 + R * K * 2 + R * 4 + R * 4
+    swbwd_bytes = R * N1 * 2 * 2 + R * I * 2  # read H, write dH, read dA
 
     if int(status.item()) != 0:
         raise RuntimeError("device status %d after the timed region" % int(status.item()))
@@ -479,18 +496,19 @@ def run_gg(args, cfg):
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": _config_dict(cfg, ws),
-            "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (GEMM1 forward, dense TMA operands)",
+            "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel (GEMM1 forward + fused SwiGLU, dense TMA operands)",
                          "achieved": achieved, "peak": tflops_sus, "unit": "TFLOP/s",
                          "frac": achieved / tflops_sus, "peak_source": src_kind + " bf16 sustained",
                          "frac_of_burst_peak": achieved / tflops_burst, "burst_peak": tflops_burst,
                          "traffic": _roofline_traffic(), "traffic_unit": "bytes per launch",
-                         "algorithmic_bytes": (R * K + E * N1 * K + R * N1) * 2},
+                         "algorithmic_bytes": (R * K + E * N1 * K + R * N1 + R * N1 // 2) * 2},
             "gemm": {"tflops_all_gemm_launches": sum(passes.values()) / (gemm_ms * 1e-3) / 1e12,
                      "frac_of_peak": sum(passes.values()) / (gemm_ms * 1e-3) / 1e12 / tflops_sus,
                      "ms": {n: per[n] for n in passes}},
             "hbm_movers": {"permute_GBps": perm_bytes / (per["permute"] * 1e-3) / 1e9,
                            "permute_dY_GBps": permdy_bytes / (per["permute_dY"] * 1e-3) / 1e9,
                            "combine_bwd_GBps": combbwd_bytes / (per["combine_bwd"] * 1e-3) / 1e9,
+                           "swiglu_bwd_GBps": swbwd_bytes / (per["swiglu_bwd"] * 1e-3) / 1e9,
                            "combine_GBps": comb_bytes / (per["combine"] * 1e-3) / 1e9,
                            "peak_GBps": hbm, "peak_source": src_kind,
                            "permute_frac": perm_bytes / (per["permute"] * 1e-3) / 1e9 / hbm,
@@ -505,6 +523,7 @@ def run_gg(args, cfg):
         if not args.no_cpu_baseline and ws == 1:
             from oracle import oracle as orc
             orc.build()
+            add_oracle_operands(cfg, host)
             ro = orc.route(host["ids"], T, k, E)
             rng = np.random.default_rng(99)
             dt, fl, desc = oracle_sample(cfg, host, ro, args.cpu_rows, rng)

@@ -183,6 +183,27 @@ int gg_forward(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
                int64_t N, int64_t K, int permute_x, int permute_y, int fuse_mul_post,
                gg_bf16* Y, int32_t* status, void* stream);
 
+/* ------------------------------------------------------ forward + SwiGLU --
+ * The forward grouped GEMM with the gated activation fused into its epilogue
+ * ([V] FusedActivation with reduction_n = 2: each pair of adjacent output
+ * columns reduces to one).  Output columns are interleaved gate/up:
+ *   y   = as gg_forward (no scatter, no scale)          [R, N]
+ *   A[i, c] = bf16( silu(y[2c]) * y[2c+1] )             [R, N/2], from the fp32 y
+ *   silu(g) = g / (1 + exp(-g))
+ *  Y [R, N] bf16 out, or NULL to store only the activation (inference);
+ *  training keeps Y for gg_swiglu_bwd.  N must be a multiple of 16. */
+int gg_forward_swiglu(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
+                      const int32_t* gather_idx, int64_t T, int topk, int E, int64_t N, int64_t K,
+                      int permute_x, gg_bf16* Y, gg_bf16* A, int32_t* status, void* stream);
+
+/* Gradient of that activation: from the stored H = y [rows, 2I] and
+ * dA = dL/dA [rows, I] (bf16), with s = 1 / (1 + exp(-g)):
+ *   dH[r, 2c]   = dA * u * s * (1 + g * (1 - s))      (gate)
+ *   dH[r, 2c+1] = dA * g * s                            (up)
+ * dH [rows, 2I] bf16 out.  I must be a multiple of 8. */
+int gg_swiglu_bwd(const gg_bf16* H, const gg_bf16* dA, int64_t rows, int64_t I, gg_bf16* dH,
+                  void* stream);
+
 /* ------------------------------------------------------------ backward dX --
  * Gradient of the forward's input ([U] grouped_gemm_dX; GroupedGemm.backward):
  *   for every expert-order row i of expert e:

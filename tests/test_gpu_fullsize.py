@@ -168,6 +168,35 @@ def test_full_layer_sampled(name):
             assert (res["dW2"][e] == 0).all()
 
 
+def test_mlp8_gemm1_swiglu_sampled():
+    """GEMM1 of mlp8 with the fused SwiGLU (the benchmark's forward), and the
+    SwiGLU backward, on sampled rows."""
+    cfg = synth.MLP8
+    T, k, E, K, N1, R = cfg.T, cfg.topk, cfg.E, cfg.K, cfg.N1, cfg.R
+    ids, w = synth.route_choices(cfg)
+    host = synth.moe_tensors(cfg, ("X", "W1"))
+    st = status_tensor()
+    dev = torch.device("cuda:0")
+    r = gg.route_hist_offsets(torch.from_numpy(ids).to(dev), E, status=st)
+    Xp = gg.permute(dbf(host["X"]), r["row_id_map"], k, status=st)
+    H, A = gg.forward_swiglu(Xp, dbf(host["W1"]), r["m_sizes"], r["gather_idx"], k, status=st)
+    dA = synth.normal_bf16(5, "mlp8/dA", (R, N1 // 2), 0.02)
+    dH = gg.swiglu_bwd(H, dbf(dA))
+    Hh, Ah, dHh = hbf(H), hbf(A), hbf(dH)
+    assert status_of(st) == 0
+    ro = orc.route(ids, T, k, E)
+    rows = _sample_rows(ro["offsets"], np.random.default_rng(7), n_random=24)
+    vals, dest = orc.forward_rows(host["X"], host["W1"], ro["m_sizes"], ro["gather_idx"], None, k,
+                                  1, 0, 0, rows)
+    assert_close(Hh[dest], vals, "mlp8 GEMM1 fwd (swiglu kernel) H")
+    assert_close(Ah[dest], orc.swiglu(vals), "mlp8 GEMM1 fwd SwiGLU act")
+    # backward from the stored H (the kernel's own input here is the GPU's H; the
+    # oracle gets the same stored rows only through its own forward, rounded)
+    Href = orc.round_bf16(vals)
+    assert_close(dHh[dest], orc.swiglu_bwd(Href, dA[dest]), "mlp8 SwiGLU bwd",
+                 magnitude=np.abs(orc.swiglu_bwd(Href, dA[dest])) * 4)
+
+
 def test_tiny_full():
     """The tiny workload end to end, every element (the oracle runs it in full)."""
     cfg = synth.TINY

@@ -222,6 +222,34 @@ def test_backward_dW(shape, px, py):
         assert (hbf(dW)[e] == 0).all()
 
 
+@pytest.mark.parametrize("px,store_y", [(0, True), (1, True), (1, False)])
+@pytest.mark.parametrize("T,topk,E,K,N", [(200, 2, 5, 320, 528), (64, 2, 4, 128, 256), (301, 3, 7, 136, 272)])
+def test_forward_swiglu(T, topk, E, K, N, px, store_y):
+    ids, w, ro = _problem(T, topk, E, K, N, (1,), 61 + T)
+    R = T * topk
+    X = synth.normal_bf16(11, "sx", (T if px else R, K), 0.1)
+    W = synth.normal_bf16(12, "sw", (E, N, K), 0.1)
+    r = _route_gpu(ids, E)
+    st = status_tensor()
+    Y, A = gg.forward_swiglu(dbf(X), dbf(W), r["m_sizes"], r["gather_idx"], topk, bool(px),
+                             store_y=store_y, status=st)
+    assert status_of(st) == 0
+    ref = orc.forward(X, W, ro["m_sizes"], ro["gather_idx"], None, T, topk, px, 0, 0)
+    if store_y:
+        assert_close(hbf(Y), ref, "forward_swiglu Y")
+    else:
+        assert Y is None
+    assert_close(hbf(A), orc.swiglu(ref), "forward_swiglu act")
+
+
+@pytest.mark.parametrize("rows,I", [(1, 8), (333, 64), (1000, 776)])
+def test_swiglu_bwd(rows, I):
+    H = synth.normal_bf16(13, "sh", (rows, 2 * I), 1.0)
+    dA = synth.normal_bf16(14, "sda", (rows, I), 0.25)
+    dH = gg.swiglu_bwd(dbf(H), dbf(dA))
+    assert_close(hbf(dH), orc.swiglu_bwd(H, dA), "swiglu bwd")
+
+
 @pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])
 @pytest.mark.parametrize("dims", [(136, 72, 200, 264, 512), (512, 256, 1024, 2048, 4096), (8, 0, 64, 8, 16)])
 def test_dual_asym(ta, tb, dims):

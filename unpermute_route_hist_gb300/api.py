@@ -140,6 +140,35 @@ def forward(X, W, m_sizes, gather_idx, topk_w, topk: int, permute_x=False, permu
     return Y
 
 
+def forward_swiglu(X, W, m_sizes, gather_idx, topk: int, permute_x=False, *, store_y=True, out=None,
+                   out_act=None, status=None):
+    """(Y [R, N] or None, A [R, N/2]): forward with the SwiGLU of interleaved gate/up columns."""
+    _need(X, torch.bfloat16, "X")
+    _need(W, torch.bfloat16, "W")
+    E, N, K = W.shape
+    _need(m_sizes, torch.int32, "m_sizes", (E,))
+    rows = X.shape[0]
+    T = rows if permute_x else rows // topk
+    R = T * topk
+    _opt(gather_idx, torch.int32, "gather_idx", (R,))
+    Y = _out(out, (R, N), torch.bfloat16, X.device, "out") if store_y else None
+    A = _out(out_act, (R, N // 2), torch.bfloat16, X.device, "out_act")
+    rc = _lib.load().gg_forward_swiglu(_p(X), _p(W), _p(m_sizes), _p(gather_idx), T, topk, E, N, K,
+                                       int(permute_x), _p(Y), _p(A), _p(status), _stream(X.device))
+    _lib.check("gg_forward_swiglu", rc)
+    return Y, A
+
+
+def swiglu_bwd(H, dA, *, out=None):
+    _need(H, torch.bfloat16, "H")
+    rows, two_i = H.shape
+    _need(dA, torch.bfloat16, "dA", (rows, two_i // 2))
+    dH = _out(out, (rows, two_i), torch.bfloat16, H.device, "out")
+    rc = _lib.load().gg_swiglu_bwd(_p(H), _p(dA), rows, two_i // 2, _p(dH), _stream(H.device))
+    _lib.check("gg_swiglu_bwd", rc)
+    return dH
+
+
 def backward_dX(dY, W, m_sizes, gather_idx, T: int, topk: int, permute_x=False, permute_y=False,
                 *, token_sum=False, out=None, out_tok=None, status=None):
     _need(dY, torch.bfloat16, "dY")

@@ -20,6 +20,8 @@ int permute_launch(const uint16_t* X, const int32_t* row_id_map, int64_t T, int 
                    uint16_t* Xp, int32_t* status, cudaStream_t stream);
 int combine_launch(const uint16_t* Y, const int32_t* row_id_map, const float* topk_w, int64_t T,
                    int topk, int64_t N, uint16_t* out, int32_t* status, cudaStream_t stream);
+int swiglu_bwd_launch(const uint16_t* H, const uint16_t* dA, int64_t rows, int64_t I, uint16_t* dH,
+                      cudaStream_t stream);
 int combine_bwd_launch(const uint16_t* G, const uint16_t* Y, const int32_t* row_id_map,
                        const float* topk_w, int64_t T, int topk, int64_t N, uint16_t* dY, float* dw,
                        int32_t* status, cudaStream_t stream);
@@ -223,6 +225,16 @@ int gg_unpermute_combine_bwd(const gg_bf16* G, const gg_bf16* Y, const int32_t* 
     if (!al16(G) || !al16(dY) || (Y && !al16(Y))) return GG_ERR_UNSUPPORTED;
     return check_launch(combine_bwd_launch(G, dw ? Y : nullptr, row_id_map, topk_w, T, topk, N, dY,
                                            dw, status, as_stream(stream)));
+}
+
+int gg_swiglu_bwd(const gg_bf16* H, const gg_bf16* dA, int64_t rows, int64_t I, gg_bf16* dH,
+                  void* stream) {
+    if (rows < 0 || I < 0) return GG_ERR_INVALID_ARG;
+    if (I % 8) return GG_ERR_UNSUPPORTED;
+    if (rows == 0 || I == 0) return GG_OK;
+    if (!H || !dA || !dH) return GG_ERR_INVALID_ARG;
+    if (!al16(H) || !al16(dA) || !al16(dH)) return GG_ERR_UNSUPPORTED;
+    return check_launch(swiglu_bwd_launch(H, dA, rows, I, dH, as_stream(stream)));
 }
 
 int gg_selftest_bounded_wait(int32_t* status, int32_t* result, uint64_t limit_ns, void* stream) {

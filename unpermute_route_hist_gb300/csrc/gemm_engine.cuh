@@ -80,6 +80,10 @@ struct GemmParams {
     int64_t ld_out;
     int scatter_out;         // RAGGED_M: store row gather_idx[i] instead of i
     const float* scale;      // RAGGED_M: multiply row i by scale[gather_idx[i]]
+    // RAGGED_M: also (or only, when out is null) store the gated activation of
+    // each pair of adjacent output columns, act[c] = silu(y[2c]) * y[2c+1]
+    uint16_t* act_out;
+    int64_t ld_act;
     DualProblem dual[2];
     int32_t* status;
 };
@@ -583,7 +587,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     dest = ti.row0 + r;
                 }
             }
-            uint16_t* orow = dest >= 0 ? out + dest * ld : nullptr;
+            uint16_t* orow = (dest >= 0 && out) ? out + dest * ld : nullptr;
+            uint16_t* arow_out = (KIND == KIND_RAGGED_M && dest >= 0 && p.act_out) ? p.act_out + dest * p.ld_act : nullptr;
             if (ti.nkb == 0) {
                 if (orow) {
                     for (int c = ti.n0; c < min(ti.n0 + kBN, ncols); c += 8)
@@ -613,6 +618,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                             o.z = pack_bf16x2(__uint_as_float(v[pc * 8 + 4]) * sc, __uint_as_float(v[pc * 8 + 5]) * sc);
                             o.w = pack_bf16x2(__uint_as_float(v[pc * 8 + 6]) * sc, __uint_as_float(v[pc * 8 + 7]) * sc);
                             *reinterpret_cast<uint4*>(orow + col) = o;
+                        }
+                    }
+                }
+                if (arow_out) {
+                    // 16 gate/up pairs of this chunk -> 16 activations (two 16-byte pieces)
+#pragma unroll
+                    for (int pc = 0; pc < 2; ++pc) {
+                        if (col0 + pc * 16 < ncols) {
+                            float a[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float g = __uint_as_float(v[pc * 16 + 2 * q]);
+                                const float u = __uint_as_float(v[pc * 16 + 2 * q + 1]);
+                                a[q] = g / (1.0f + __expf(-g)) * u;
+                            }
+                            uint4 o;
+                            o.x = pack_bf16x2(a[0], a[1]);
+                            o.y = pack_bf16x2(a[2], a[3]);
+                            o.z = pack_bf16x2(a[4], a[5]);
+                            o.w = pack_bf16x2(a[6], a[7]);
+                            *reinterpret_cast<uint4*>(arow_out + col0 / 2 + pc * 8) = o;
                         }
                     }
                 }

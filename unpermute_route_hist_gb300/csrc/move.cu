@@ -8,6 +8,8 @@
 //                     over a token's slots (backend.py, unpermute; matmul_ogs.py,
 //                     matmul_ogs_torch's fp32 accumulation).  Output-stationary
 //                     and deterministic: out[t] sums its slots in slot order.
+//  swiglu backward    gradient of the gated activation over interleaved gate/up
+//                     columns (matmul_ogs.py, FusedActivation, reduction_n = 2).
 //  combine backward   its gradient (backend.py, unpermute_bwd): each slot's row
 //                     gets the token's output gradient times the slot weight,
 //                     and each weight gets <output gradient, forward row>.
@@ -178,6 +180,33 @@ combine_bwd_kernel(const uint4* __restrict__ G, const uint4* __restrict__ Y,
     }
 }
 
+// SwiGLU backward over interleaved gate/up columns: each thread takes 8
+// activations (16 bytes of dA) and the 16 matching columns of H, and writes
+// the 16 columns of dH.  Grid-stride over 8-activation groups.
+__global__ void __launch_bounds__(kMoveThreads)
+swiglu_bwd_kernel(const uint4* __restrict__ H, const uint4* __restrict__ dA, int64_t groups,
+                  uint4* __restrict__ dH) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x; i < groups;
+         i += static_cast<int64_t>(gridDim.x) * kMoveThreads) {
+        const uint4 dv = ld_stream(dA + i);
+        const uint4 h0 = ld_stream(H + 2 * i), h1 = ld_stream(H + 2 * i + 1);
+        const __nv_bfloat162* dh = reinterpret_cast<const __nv_bfloat162*>(&dv);
+        const __nv_bfloat162* hh[2] = {reinterpret_cast<const __nv_bfloat162*>(&h0),
+                                       reinterpret_cast<const __nv_bfloat162*>(&h1)};
+        uint32_t outw[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float2 gu = __bfloat1622float2(hh[q >> 2][q & 3]);  // (gate, up) of activation q
+            const float2 d2 = __bfloat1622float2(dh[q >> 1]);
+            const float d = (q & 1) ? d2.y : d2.x;
+            const float s = 1.0f / (1.0f + __expf(-gu.x));
+            outw[q] = pack_bf16x2(d * gu.y * s * (1.0f + gu.x * (1.0f - s)), d * gu.x * s);
+        }
+        dH[2 * i] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        dH[2 * i + 1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+    }
+}
+
 unsigned move_grid(int64_t rows) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -194,6 +223,18 @@ int permute_launch(const uint16_t* X, const int32_t* row_id_map, int64_t T, int 
     permute_kernel<<<move_grid(T), kMoveThreads, 0, stream>>>(
         reinterpret_cast<const uint4*>(X), row_id_map, T, topk, K / 8, reinterpret_cast<uint4*>(Xp),
         R, status);
+    return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
+}
+
+int swiglu_bwd_launch(const uint16_t* H, const uint16_t* dA, int64_t rows, int64_t I, uint16_t* dH,
+                      cudaStream_t stream) {
+    const int64_t groups = rows * I / 8;
+    int64_t blocks = (groups + kMoveThreads - 1) / kMoveThreads;
+    const int64_t cap = static_cast<int64_t>(move_grid(INT64_MAX)) * 4;
+    if (blocks > cap) blocks = cap;
+    swiglu_bwd_kernel<<<static_cast<unsigned>(blocks), kMoveThreads, 0, stream>>>(
+        reinterpret_cast<const uint4*>(H), reinterpret_cast<const uint4*>(dA), groups,
+        reinterpret_cast<uint4*>(dH));
     return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
 }
 
