@@ -601,12 +601,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             if (!warp_wait(&ctl->tmem_full[buf], acc_phase, abort_flag, p.status, 64)) break;
             tc_fence_after();
             const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN;
-#pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(taddr0 + c * 32, v);
-                tmem_ld_wait();
-                const int col0 = ti.n0 + c * 32;
+            // convert and store 32 accumulator columns starting at output column col0
+            auto store_chunk = [&](const uint32_t (&v)[32], int col0) {
                 if (orow) {
 #pragma unroll
                     for (int pc = 0; pc < 4; ++pc) {
@@ -628,10 +624,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         if (col0 + pc * 16 < ncols) {
                             float a[8];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const float g = __uint_as_float(v[pc * 16 + 2 * q]);
-                                const float u = __uint_as_float(v[pc * 16 + 2 * q + 1]);
-                                a[q] = g / (1.0f + __expf(-g)) * u;
+                            for (int qq = 0; qq < 8; ++qq) {
+                                const float g = __uint_as_float(v[pc * 16 + 2 * qq]);
+                                const float u = __uint_as_float(v[pc * 16 + 2 * qq + 1]);
+                                a[qq] = g / (1.0f + __expf(-g)) * u;
                             }
                             uint4 o;
                             o.x = pack_bf16x2(a[0], a[1]);
@@ -642,10 +638,31 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         }
                     }
                 }
+            };
+            // Four 32-column TMEM loads per wait: the loads' latency is paid once per
+            // 128 columns.  The accumulator is handed back to the MMA warp as soon as
+            // the last load has landed in registers, before its columns are stored.
+            constexpr int kColsPerWait = 128;
+#pragma unroll 1
+            for (int c = 0; c < kBN / kColsPerWait; ++c) {
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                const uint32_t ta = taddr0 + c * kColsPerWait;
+                tmem_ld_32x32b_x32(ta, v0);
+                tmem_ld_32x32b_x32(ta + 32, v1);
+                tmem_ld_32x32b_x32(ta + 64, v2);
+                tmem_ld_32x32b_x32(ta + 96, v3);
+                tmem_ld_wait();
+                if (c == kBN / kColsPerWait - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->tmem_empty[buf]);
+                }
+                const int col0 = ti.n0 + c * kColsPerWait;
+                store_chunk(v0, col0);
+                store_chunk(v1, col0 + 32);
+                store_chunk(v2, col0 + 64);
+                store_chunk(v3, col0 + 96);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->tmem_empty[buf]);
             ++acc_count;
         }
     } else {
