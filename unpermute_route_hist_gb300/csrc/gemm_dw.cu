@@ -56,5 +56,5 @@ extern "C" int gg_backward_dW(const gg_bf16* X, const gg_bf16* dY, const int32_t
         return launch_gemm<KIND_RAGGED_K, true, true, true, false, false>(mA, mB, mA, mB, p, bound, st);
     if (permute_x)
         return launch_gemm<KIND_RAGGED_K, true, true, false, true, false>(mA, mB, mA, mB, p, bound, st);
-    return launch_gemm<KIND_RAGGED_K, true, true, false, false, false>(mA, mB, mA, mB, p, bound, st);
+    return launch_gemm<KIND_RAGGED_K, true, true, false, false, true>(mA, mB, mA, mB, p, bound, st);
 }

@@ -9,14 +9,18 @@
 // (interface.py: grouped_gemm_forward / _dX / _dW; matmul_ogs.py: the ragged
 // dw comment; backend.py: asym_dual_gmm_separated.)
 //
-// Tile: 128 x 256 output, reduction blocks of kBK, a kStages-deep shared-memory ring,
-// optionally (PAIR) run by 2-CTA clusters on adjacent m-tiles that share the
-// B tile: each CTA TMA-loads half of it and multicasts it to both, and a stage
-// is released only when both CTAs' MMAs have read it;
-// fp32 accumulators in tensor memory (two 256-column buffers so the epilogue
-// of one tile overlaps the main loop of the next).  Warp roles:
+// Tile: 128 x 256 output, reduction blocks of kBK, a shared-memory ring of
+// operand stages, fp32 accumulators in tensor memory (two 256-column buffers
+// so the epilogue of one tile overlaps the main loop of the next).
+// PAIR: 2-CTA clusters run the cta_group::2 MMA on a 256 x 256 tile made of two
+// adjacent m-tiles of the same expert and n-tile.  Each CTA holds its own A
+// rows and one half of the B columns (32 KB a stage instead of 48, so six
+// stages fit), the even CTA issues the MMA for both, and each CTA's tensor
+// memory holds the accumulator of its own 128 rows.  Warp roles:
 //   warp 0      tile scheduler + TMA producer (lane 0) for dense operands
 //   warp 1      TMEM allocation + MMA issue (lane 0); zeroes ragged tails
+//               (PAIR, odd CTA: zeroes its own ragged tails and forwards the
+//               stage's readiness to the even CTA)
 //   warps 2-5   epilogue: TMEM -> registers -> scale -> bf16 -> global rows
 //   warps 6-9   (only with a gathered operand) cp.async row-gather producers;
 //               each thread's copies arrive on the stage barrier as they land
@@ -38,13 +42,11 @@ namespace gg {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;                  // reduction block (32 or 64)
-constexpr int kStages = 4;               // 192 KB of operand stages
+constexpr int kMaxStages = 6;
 // K-major tiles: rows of kBK bf16 (kKRowBytes), swizzled over the row width
 constexpr int kKRowBytes = kBK * 2;
 constexpr int kKChunks = kKRowBytes / 16;  // 16-byte chunks per K-major row
 constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = kBN * kBK * 2;
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators
 constexpr int kGroupM = 16;             // m-tiles per raster group (L2 reuse)
 constexpr int kGatherWarps = 4;
@@ -99,8 +101,9 @@ struct TileInfo {
 };
 
 struct SharedCtl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t pfull[kMaxStages];  // PAIR dW, even CTA: the odd CTA's tail stage is ready
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t drain;
@@ -113,8 +116,8 @@ struct SharedCtl {
 // Tiles are scheduled in "units": one m-tile, or (PAIR) two adjacent m-tiles
 // of the same expert / problem and n-tile that a 2-CTA cluster computes
 // together, CTA rank r taking m-tile 2*unit + r.  A rank whose m-tile falls
-// past the end gets rows <= 0 (a phantom tile: it loads and releases its half
-// of the shared operand but computes and stores nothing).
+// past the end gets rows <= 0 (a phantom tile: it still loads its operand
+// boxes, its accumulator rows are computed and handed back, nothing is stored).
 template <int KIND, bool PAIR>
 __device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
                                                 const int32_t* s_off, const int32_t* s_tp,
@@ -215,21 +218,33 @@ __device__ __forceinline__ int64_t gather_row(const GemmParams& p, const GatherS
 
 template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR>
 struct GemmTraits {
-    static_assert(!(PAIR && B_GATHER), "the shared (multicast) operand is loaded by TMA");
+    static_assert(!(PAIR && (A_GATHER || B_GATHER)), "2-CTA tiles are loaded by TMA only");
+    static_assert(!(PAIR && KIND == KIND_DUAL), "the dual GEMM runs on single CTAs");
     static constexpr bool kAnyGather = A_GATHER || B_GATHER;
     static constexpr int kThreads = 32 * (6 + (kAnyGather ? kGatherWarps : 0));
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+    static constexpr int kStages = PAIR ? 6 : 4;
+    static constexpr int kBRows = PAIR ? kBN / 2 : kBN;  // B tile rows (n) held by one CTA
+    static constexpr uint32_t kBBytes = kBRows * kBK * 2;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, kBN, A_MN ? 1 : 0, B_MN ? 1 : 0);
     static constexpr uint32_t kTmaBytes = (A_GATHER ? 0u : kABytes) + (B_GATHER ? 0u : kBBytes);
     static constexpr uint32_t kFullCount = 1 + (kAnyGather ? kGatherWarps * 32 : 0);
-    // a stage is free once every CTA that reads the shared operand released it
-    static constexpr uint32_t kEmptyCount = PAIR ? 2 : 1;
-    static constexpr uint16_t kPairMask = 0x3;
+    // PAIR: both CTAs' TMA bytes of a stage complete on the even CTA's barrier,
+    // except for a ragged reduction's tail stage (dW): there each CTA zeroes its
+    // own tail rows before the MMA, so the odd CTA's copies complete on its own
+    // barrier and the odd CTA then signals the even one (pfull).
+    static constexpr bool kTailFwd = PAIR && KIND == KIND_RAGGED_K;
+    static_assert(kStages <= kMaxStages, "stage ring");
 };
 
+template <bool PAIR>
 __host__ __device__ constexpr size_t gemm_smem_bytes(int E) {
-    return 1024 /* alignment slack */ + static_cast<size_t>(kStages) * kStageBytes +
+    return 1024 /* alignment slack */ +
+           static_cast<size_t>(PAIR ? 6 : 4) * (kABytes + (PAIR ? kBN / 2 : kBN) * kBK * 2) +
            sizeof(SharedCtl) + 2 * static_cast<size_t>(E + 1) * sizeof(int32_t) + 16;
 }
+static_assert(gemm_smem_bytes<true>(GG_MAX_EXPERTS) <= 227 * 1024, "shared memory (pair)");
+static_assert(gemm_smem_bytes<false>(GG_MAX_EXPERTS) <= 227 * 1024, "shared memory");
 
 // Byte offset of 16-byte chunk c of row r in a K-major tile: the swizzle XORs
 // the chunk index with address bits 7.. (128-byte rows: r & 7; 64-byte rows:
@@ -265,6 +280,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     uint8_t* stage_base = smem;
+    constexpr int kStages = Tr::kStages;
+    constexpr uint32_t kStageBytes = Tr::kStageBytes;
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kStages * kStageBytes);
     int32_t* s_off = reinterpret_cast<int32_t*>(ctl + 1);
     int32_t* s_tp = s_off + (p.E + 1);
@@ -273,6 +290,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     volatile int* abort_flag = &ctl->abort_flag;
     // persistent schedule: CTAs (or 2-CTA clusters) take units slot, slot + nslot, ...
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;  // PAIR: the CTA that issues the MMAs
     const int64_t slot = PAIR ? static_cast<int64_t>(cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
     const int64_t nslot = PAIR ? static_cast<int64_t>(nclusters_x()) : static_cast<int64_t>(gridDim.x);
 
@@ -280,11 +298,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl->full[s], Tr::kFullCount);
-            mbar_init(&ctl->empty[s], Tr::kEmptyCount);
+            mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->pfull[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tmem_full[b], 1);
-            mbar_init(&ctl->tmem_empty[b], 4);
+            // PAIR: the even CTA's barrier also counts the odd CTA's epilogue warps
+            mbar_init(&ctl->tmem_empty[b], PAIR ? 8 : 4);
         }
         mbar_init(&ctl->drain, 1);
         ctl->abort_flag = 0;
@@ -299,8 +319,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         }
     }
     if (warp == 1) {
-        tmem_alloc(&ctl->tmem_base, kTmemCols);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&ctl->tmem_base, kTmemCols);
+            tmem_relinquish();
+        }
     }
     if (warp == 2) {
         // Row offsets and (RAGGED_M) m-tile prefix of the experts: one warp,
@@ -381,62 +406,73 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
                 const CUtensorMap* mA = (KIND == KIND_DUAL && ti.e == 1) ? &tmA1 : &tmA0;
                 const CUtensorMap* mB = (KIND == KIND_DUAL && ti.e == 1) ? &tmB1 : &tmB0;
-                const bool phantom = ti.rows <= 0;
-                const uint32_t tx = (A_GATHER || phantom ? 0u : static_cast<uint32_t>(kABytes)) +
-                                    (B_GATHER ? 0u : static_cast<uint32_t>(kBBytes));
                 for (int kb = 0; kb < ti.nkb; ++kb) {
                     if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     uint8_t* sA = stage_base + stage * kStageBytes;
                     uint8_t* sB = sA + kABytes;
-                    if (tx) mbar_arrive_expect_tx(&ctl->full[stage], tx);
-                    else mbar_arrive(&ctl->full[stage]);
                     const int32_t red = static_cast<int32_t>(ti.red0 + static_cast<int64_t>(kb) * kBK);
-                    if (!A_GATHER && !phantom) {
+                    if (PAIR) {
+                        // A: this CTA's own m-tile (an odd CTA past the expert's last
+                        // m-tile still loads its box: those rows are never stored).
+                        // B: this CTA's half of the n-tile's columns.
+                        const bool tail = Tr::kTailFwd && ti.red_len - kb * kBK < kBK;
+                        uint32_t bar;
+                        if (tail) {
+                            mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
+                            bar = mapa_u32(&ctl->full[stage], rank);
+                        } else {
+                            if (leader) mbar_arrive_expect_tx(&ctl->full[stage], 2 * kStageBytes);
+                            bar = mapa_u32(&ctl->full[stage], 0);
+                        }
+                        const int32_t nb = ti.n0 + static_cast<int32_t>(rank) * (kBN / 2);
                         if (!A_MN) {
-                            tma_load_2d(sA, mA, &ctl->full[stage], red, static_cast<int32_t>(ti.row0));
+                            tma_load_2d_pair(sA, mA, bar, red, static_cast<int32_t>(ti.row0));
                         } else {
 #pragma unroll
                             for (int cc = 0; cc < kBM / 64; ++cc)
-                                tma_load_2d(sA + cc * kBK * 128, mA, &ctl->full[stage],
-                                            static_cast<int32_t>(ti.row0) + cc * 64, red);
+                                tma_load_2d_pair(sA + cc * kBK * 128, mA, bar, static_cast<int32_t>(ti.row0) + cc * 64, red);
                         }
-                    }
-                    if (!B_GATHER) {
-                        if (PAIR) {
-                            // this CTA loads half of the shared B tile into both CTAs
-                            if (!B_MN) {
-                                uint8_t* dst = sB + rank * (kBBytes / 2);
-                                const int32_t n = ti.n0 + static_cast<int32_t>(rank) * (kBN / 2);
-                                if (KIND == KIND_RAGGED_M)
-                                    tma_load_3d_mc(dst, mB, &ctl->full[stage], red, n, ti.e, Tr::kPairMask);
-                                else
-                                    tma_load_2d_mc(dst, mB, &ctl->full[stage], red, n, Tr::kPairMask);
-                            } else {
-#pragma unroll
-                                for (int h = 0; h < kBN / 128; ++h) {
-                                    const int cc = static_cast<int>(rank) * (kBN / 128) + h;
-                                    if (KIND == KIND_RAGGED_M)
-                                        tma_load_3d_mc(sB + cc * kBK * 128, mB, &ctl->full[stage],
-                                                       ti.n0 + cc * 64, red, ti.e, Tr::kPairMask);
-                                    else
-                                        tma_load_2d_mc(sB + cc * kBK * 128, mB, &ctl->full[stage],
-                                                       ti.n0 + cc * 64, red, Tr::kPairMask);
-                                }
-                            }
-                        } else if (!B_MN) {
-                            if (KIND == KIND_RAGGED_M)
-                                tma_load_3d(sB, mB, &ctl->full[stage], red, ti.n0, ti.e);
-                            else
-                                tma_load_2d(sB, mB, &ctl->full[stage], red, ti.n0);
+                        if (!B_MN) {
+                            if (KIND == KIND_RAGGED_M) tma_load_3d_pair(sB, mB, bar, red, nb, ti.e);
+                            else tma_load_2d_pair(sB, mB, bar, red, nb);
                         } else {
 #pragma unroll
-                            for (int cc = 0; cc < kBN / 64; ++cc) {
+                            for (int cc = 0; cc < Tr::kBRows / 64; ++cc) {
                                 if (KIND == KIND_RAGGED_M)
-                                    tma_load_3d(sB + cc * kBK * 128, mB, &ctl->full[stage],
-                                                ti.n0 + cc * 64, red, ti.e);
+                                    tma_load_3d_pair(sB + cc * kBK * 128, mB, bar, nb + cc * 64, red, ti.e);
                                 else
-                                    tma_load_2d(sB + cc * kBK * 128, mB, &ctl->full[stage],
-                                                ti.n0 + cc * 64, red);
+                                    tma_load_2d_pair(sB + cc * kBK * 128, mB, bar, nb + cc * 64, red);
+                            }
+                        }
+                    } else {
+                        if (Tr::kTmaBytes) mbar_arrive_expect_tx(&ctl->full[stage], Tr::kTmaBytes);
+                        else mbar_arrive(&ctl->full[stage]);
+                        if (!A_GATHER) {
+                            if (!A_MN) {
+                                tma_load_2d(sA, mA, &ctl->full[stage], red, static_cast<int32_t>(ti.row0));
+                            } else {
+#pragma unroll
+                                for (int cc = 0; cc < kBM / 64; ++cc)
+                                    tma_load_2d(sA + cc * kBK * 128, mA, &ctl->full[stage],
+                                                static_cast<int32_t>(ti.row0) + cc * 64, red);
+                            }
+                        }
+                        if (!B_GATHER) {
+                            if (!B_MN) {
+                                if (KIND == KIND_RAGGED_M)
+                                    tma_load_3d(sB, mB, &ctl->full[stage], red, ti.n0, ti.e);
+                                else
+                                    tma_load_2d(sB, mB, &ctl->full[stage], red, ti.n0);
+                            } else {
+#pragma unroll
+                                for (int cc = 0; cc < kBN / 64; ++cc) {
+                                    if (KIND == KIND_RAGGED_M)
+                                        tma_load_3d(sB + cc * kBK * 128, mB, &ctl->full[stage],
+                                                    ti.n0 + cc * 64, red, ti.e);
+                                    else
+                                        tma_load_2d(sB + cc * kBK * 128, mB, &ctl->full[stage],
+                                                    ti.n0 + cc * 64, red);
+                                }
                             }
                         }
                     }
@@ -445,122 +481,145 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 }
             }
             // Let every TMA copy this thread issued land before the CTA can exit.
-            const int64_t pend = issued < kStages ? issued : kStages;
-            int dstage = stage;
-            uint32_t dphase = phase;
-            for (int64_t j = 0; j < pend; ++j) {
-                if (--dstage < 0) { dstage = kStages - 1; dphase ^= 1u; }
-                int dummy = 0;
-                mbar_wait(&ctl->full[dstage], dphase, reinterpret_cast<volatile int*>(&dummy), p.status);
-            }
-            // With a partner CTA: acquire every slot once more, i.e. wait until both
-            // CTAs released each stage, so no remote arrival can reach this CTA's
-            // barriers after it exits.
-            if (PAIR && issued > 0) {
-                for (int j = 0; j < kStages; ++j) {
+            // (PAIR, odd CTA: its copies complete on the even CTA's barriers, or
+            // on its own tail barriers that its warp 1 waits for; the even CTA's
+            // MMAs consume all of them before the teardown's cluster barrier.)
+            if (!PAIR || leader) {
+                const int64_t pend = issued < kStages ? issued : kStages;
+                int dstage = stage;
+                uint32_t dphase = phase;
+                for (int64_t j = 0; j < pend; ++j) {
+                    if (--dstage < 0) { dstage = kStages - 1; dphase ^= 1u; }
                     int dummy = 0;
-                    mbar_wait(&ctl->empty[stage], phase ^ 1u, reinterpret_cast<volatile int*>(&dummy), p.status);
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    mbar_wait(&ctl->full[dstage], dphase, reinterpret_cast<volatile int*>(&dummy), p.status);
                 }
             }
         }
     } else if (warp == 1) {
-        // --------------------------------------------------- MMA issuer --
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t acc_count = 0;
-        bool ok = true, any_mma = false;
-        for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
-            const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
-            if (ti.nkb == 0) continue;
-            if (PAIR && ti.rows <= 0) {
-                // phantom tile: only release each stage to both CTAs once it landed
+        // Rows [valid, zr_end) of a stage's dense operands hold the next expert's
+        // reduction rows: overwrite them with zeros (both operands, so no 0 * inf).
+        auto zero_tail = [&](int stage, int valid, int zr_end) {
+            const int nz = zr_end - valid;
+            if (nz <= 0) return;
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            uint8_t* st = stage_base + stage * kStageBytes;
+            if (!A_GATHER) {
+                for (int idx = lane; idx < nz * (kBM / 64) * 8; idx += 32) {
+                    const int piece = idx & 7, rest = idx >> 3;
+                    const int cc = rest % (kBM / 64), r = valid + rest / (kBM / 64);
+                    *reinterpret_cast<uint4*>(st + cc * kBK * 128 + r * 128 + piece * 16) = z;
+                }
+            }
+            if (!B_GATHER) {
+                for (int idx = lane; idx < nz * (Tr::kBRows / 64) * 8; idx += 32) {
+                    const int piece = idx & 7, rest = idx >> 3;
+                    const int cc = rest % (Tr::kBRows / 64), r = valid + rest / (Tr::kBRows / 64);
+                    *reinterpret_cast<uint4*>(st + kABytes + cc * kBK * 128 + r * 128 + piece * 16) = z;
+                }
+            }
+            fence_proxy_async_smem();
+        };
+        if (!PAIR || leader) {
+            // ----------------------------------------------- MMA issuer --
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t pfull_par = 0;  // per-slot parity of pfull (tail stages only)
+            uint32_t acc_count = 0;
+            bool ok = true, any_mma = false;
+            for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
+                const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
+                if (ti.nkb == 0) continue;
+                const uint32_t buf = acc_count & 1u;
+                const uint32_t acc_phase = (acc_count >> 1) & 1u;
+                if (!warp_wait(&ctl->tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.status, 0, PAIR)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * kBN;
                 for (int kb = 0; kb < ti.nkb; ++kb) {
                     if (!warp_wait(&ctl->full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sA = stage0 + stage * kStageBytes;
+                    const uint32_t sB = sA + kABytes;
+                    int ksteps = kBK / 16;
+                    if (KIND == KIND_RAGGED_K) {
+                        const int valid = min(kBK, ti.red_len - kb * kBK);
+                        if (valid < kBK) {
+                            ksteps = (valid + 15) / 16;
+                            zero_tail(stage, valid, ksteps * 16);
+                            __syncwarp();
+                            if (Tr::kTailFwd) {
+                                // the odd CTA's half of this stage has landed, tail zeroed
+                                if (!warp_wait(&ctl->pfull[stage], (pfull_par >> stage) & 1u, abort_flag, p.status, 0, true)) {
+                                    ok = false;
+                                    break;
+                                }
+                                pfull_par ^= 1u << stage;
+                                tc_fence_after();
+                            }
+                        }
+                    }
                     if (lane == 0) {
-                        mbar_arrive_cluster(&ctl->empty[stage], 0);
-                        mbar_arrive_cluster(&ctl->empty[stage], 1);
+                        // cp.async writes are generic-proxy; order them before the
+                        // tensor core's async-proxy reads of this stage
+                        if (Tr::kAnyGather) fence_proxy_async_smem();
+                        for (int ks = 0; ks < ksteps; ++ks) {
+                            const uint64_t ad = operand_desc<A_MN>(sA, ks), bd = operand_desc<B_MN>(sB, ks);
+                            const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+                            if (PAIR) umma_bf16_pair(d_tmem, ad, bd, Tr::kIdesc, acc);
+                            else umma_bf16(d_tmem, ad, bd, Tr::kIdesc, acc);
+                        }
+                        if (PAIR) umma_commit_pair(&ctl->empty[stage], 0x3);
+                        else umma_commit(&ctl->empty[stage]);
+                        any_mma = true;
                     }
                     __syncwarp();
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
-                continue;
-            }
-            const uint32_t buf = acc_count & 1u;
-            const uint32_t acc_phase = (acc_count >> 1) & 1u;
-            if (!warp_wait(&ctl->tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + buf * kBN;
-            for (int kb = 0; kb < ti.nkb; ++kb) {
-                if (!warp_wait(&ctl->full[stage], phase, abort_flag, p.status)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t sA = stage0 + stage * kStageBytes;
-                const uint32_t sB = sA + kABytes;
-                int ksteps = kBK / 16;
-                if (KIND == KIND_RAGGED_K) {
-                    const int valid = min(kBK, ti.red_len - kb * kBK);
-                    if (valid < kBK) {
-                        ksteps = (valid + 15) / 16;
-                        const int zr_end = ksteps * 16;
-                        // rows [valid, zr_end) of dense (TMA) operands hold the next
-                        // expert's rows: overwrite them with zeros.
-                        const int nz = zr_end - valid;
-                        if (nz > 0) {
-                            const uint4 z = make_uint4(0, 0, 0, 0);
-                            if (!A_GATHER) {
-                                for (int idx = lane; idx < nz * (kBM / 64) * 8; idx += 32) {
-                                    const int piece = idx & 7, rest = idx >> 3;
-                                    const int cc = rest % (kBM / 64), r = valid + rest / (kBM / 64);
-                                    *reinterpret_cast<uint4*>(stage_base + stage * kStageBytes + cc * kBK * 128 + r * 128 + piece * 16) = z;
-                                }
-                            }
-                            if (!B_GATHER) {
-                                for (int idx = lane; idx < nz * (kBN / 64) * 8; idx += 32) {
-                                    const int piece = idx & 7, rest = idx >> 3;
-                                    const int cc = rest % (kBN / 64), r = valid + rest / (kBN / 64);
-                                    *reinterpret_cast<uint4*>(stage_base + stage * kStageBytes + kABytes + cc * kBK * 128 + r * 128 + piece * 16) = z;
-                                }
-                            }
-                            fence_proxy_async_smem();
-                        }
-                        __syncwarp();
-                    }
-                }
+                if (!ok) break;
                 if (lane == 0) {
-                    // cp.async writes are generic-proxy; order them before the
-                    // tensor core's async-proxy reads of this stage
-                    if (Tr::kAnyGather) fence_proxy_async_smem();
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        umma_bf16(d_tmem, operand_desc<A_MN>(sA, ks), operand_desc<B_MN>(sB, ks),
-                                  Tr::kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
-                    }
-                    if (PAIR) umma_commit_mc(&ctl->empty[stage], Tr::kPairMask);
-                    else umma_commit(&ctl->empty[stage]);
-                    any_mma = true;
+                    if (PAIR) umma_commit_pair(&ctl->tmem_full[buf], 0x3);
+                    else umma_commit(&ctl->tmem_full[buf]);
                 }
                 __syncwarp();
-                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                ++acc_count;
             }
-            if (!ok) break;
-            if (lane == 0) umma_commit(&ctl->tmem_full[buf]);
+            // All MMAs of this thread finish before TMEM is released.
+            if (lane == 0 && any_mma) {
+                if (PAIR) umma_commit_pair(&ctl->drain, 0x1);
+                else umma_commit(&ctl->drain);
+                int dummy = 0;
+                mbar_wait(&ctl->drain, 0, reinterpret_cast<volatile int*>(&dummy), p.status);
+            }
             __syncwarp();
-            ++acc_count;
+        } else if (Tr::kTailFwd) {
+            // --------------------- odd CTA of a dW pair: tail stages only --
+            int stage = 0;
+            uint32_t full_par = 0;  // per-slot parity of this CTA's own full barriers
+            bool ok = true;
+            for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
+                const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
+                for (int kb = 0; kb < ti.nkb; ++kb) {
+                    const int valid = min(kBK, ti.red_len - kb * kBK);
+                    if (valid < kBK) {
+                        if (!warp_wait(&ctl->full[stage], (full_par >> stage) & 1u, abort_flag, p.status)) { ok = false; break; }
+                        full_par ^= 1u << stage;
+                        zero_tail(stage, valid, ((valid + 15) / 16) * 16);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(&ctl->pfull[stage], 0);
+                        __syncwarp();
+                    }
+                    if (++stage == kStages) stage = 0;
+                }
+            }
         }
-        // All MMAs of this thread finish before TMEM is released.
-        if (lane == 0 && any_mma) {
-            umma_commit(&ctl->drain);
-            int dummy = 0;
-            mbar_wait(&ctl->drain, 0, reinterpret_cast<volatile int*>(&dummy), p.status);
-        }
-        __syncwarp();
     } else if (warp < 6) {
         // ----------------------------------------------------- epilogue --
         const int q = warp & 3;        // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;   // tile row of this thread
         uint32_t acc_count = 0;
         for (int64_t t = slot; t < total_tiles; t += nslot) {
+            // (PAIR: an odd CTA past its expert's last m-tile has rows <= 0; it
+            // still takes part in the accumulator hand-off but stores nothing.)
             const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
-            if (ti.rows <= 0) continue;  // phantom tile: nothing to store
             const int ncols = tile_cols<KIND>(p, ti.e);
             // destination row, scale, output base
             uint16_t* out = p.out;
@@ -598,8 +657,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             }
             const uint32_t buf = acc_count & 1u;
             const uint32_t acc_phase = (acc_count >> 1) & 1u;
-            if (!warp_wait(&ctl->tmem_full[buf], acc_phase, abort_flag, p.status, 64)) break;
+            if (!warp_wait(&ctl->tmem_full[buf], acc_phase, abort_flag, p.status, 64, PAIR)) break;
             tc_fence_after();
+            // hand the accumulator back to the MMA issuer (the even CTA's, for a pair)
+            auto release_acc = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (PAIR) mbar_arrive_cluster(&ctl->tmem_empty[buf], 0);
+                    else mbar_arrive(&ctl->tmem_empty[buf]);
+                }
+            };
+            if (ti.rows <= 0) {
+                release_acc();
+                ++acc_count;
+                continue;
+            }
             const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN;
             // convert and store 32 accumulator columns starting at output column col0
             auto store_chunk = [&](const uint32_t (&v)[32], int col0) {
@@ -652,11 +725,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 tmem_ld_32x32b_x32(ta + 64, v2);
                 tmem_ld_32x32b_x32(ta + 96, v3);
                 tmem_ld_wait();
-                if (c == kBN / kColsPerWait - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->tmem_empty[buf]);
-                }
+                if (c == kBN / kColsPerWait - 1) release_acc();
                 const int col0 = ti.n0 + c * kColsPerWait;
                 store_chunk(v0, col0);
                 store_chunk(v1, col0 + 32);
@@ -809,7 +878,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     __syncthreads();
     if (PAIR) cluster_sync();  // neither CTA leaves while the other may still signal it
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+    if (warp == 1) {
+        if (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
+        else tmem_dealloc(tmem_base, kTmemCols);
+    }
 }
 
 // ------------------------------------------------------------------ host --
@@ -826,9 +898,9 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
                 const CUtensorMap& b1, const GemmParams& p, int64_t tile_bound, cudaStream_t stream) {
     using Tr = GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>;
     auto kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>;
-    const size_t smem = gemm_smem_bytes(p.E);
+    const size_t smem = gemm_smem_bytes<PAIR>(p.E);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(gemm_smem_bytes(GG_MAX_EXPERTS)));
+                                         static_cast<int>(gemm_smem_bytes<PAIR>(GG_MAX_EXPERTS)));
     if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
     const int64_t sms = num_sms();
     if (tile_bound < 1) tile_bound = 1;

@@ -66,15 +66,16 @@ int gg_forward(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
     p.scatter_out = permute_y ? 1 : 0;
     p.scale = fuse_mul_post ? topk_w : nullptr;
     CUtensorMap mA{}, mB{};
-    if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN)) return GG_ERR_CUDA;
     const int64_t bound = row_tile_bound(R, E) * ((N + kBN - 1) / kBN);
     if (permute_x) {
+        if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN)) return GG_ERR_CUDA;
         p.ga = GatherSrc{X, K, T, K, ROW_TOKEN};
-        mA = mB;  // unused
-        return launch_gemm<KIND_RAGGED_M, false, false, true, false, false>(mA, mB, mA, mB, p, bound, st);
+        return launch_gemm<KIND_RAGGED_M, false, false, true, false, false>(mB, mB, mB, mB, p, bound, st);
     }
+    // 2-CTA tiles: each CTA loads half of the 256 W rows of an n-tile
+    if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN / 2)) return GG_ERR_CUDA;
     if (!encode_map_2d(&mA, X, K, R, K, kBK, kBM)) return GG_ERR_CUDA;
-    return launch_gemm<KIND_RAGGED_M, false, false, false, false, false>(mA, mB, mA, mB, p, bound, st);
+    return launch_gemm<KIND_RAGGED_M, false, false, false, false, true>(mA, mB, mA, mB, p, bound, st);
 }
 
 int gg_forward_swiglu(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
@@ -104,14 +105,15 @@ int gg_forward_swiglu(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes
     p.act_out = A;
     p.ld_act = N / 2;
     CUtensorMap mA{}, mB{};
-    if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN)) return GG_ERR_CUDA;
     const int64_t bound = row_tile_bound(R, E) * ((N + kBN - 1) / kBN);
     if (permute_x) {
+        if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN)) return GG_ERR_CUDA;
         p.ga = GatherSrc{X, K, T, K, ROW_TOKEN};
         return launch_gemm<KIND_RAGGED_M, false, false, true, false, false>(mB, mB, mB, mB, p, bound, st);
     }
+    if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN / 2)) return GG_ERR_CUDA;
     if (!encode_map_2d(&mA, X, K, R, K, kBK, kBM)) return GG_ERR_CUDA;
-    return launch_gemm<KIND_RAGGED_M, false, false, false, false, false>(mA, mB, mA, mB, p, bound, st);
+    return launch_gemm<KIND_RAGGED_M, false, false, false, false, true>(mA, mB, mA, mB, p, bound, st);
 }
 
 int gg_backward_dX(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes,
@@ -149,7 +151,7 @@ int gg_backward_dX(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes,
             rc = launch_gemm<KIND_RAGGED_M, false, true, true, false, false>(mB, mB, mB, mB, p, bound, st);
         } else {
             if (!encode_map_2d(&mA, dY, N, R, N, kBK, kBM)) return GG_ERR_CUDA;
-            rc = launch_gemm<KIND_RAGGED_M, false, true, false, false, false>(mA, mB, mA, mB, p, bound, st);
+            rc = launch_gemm<KIND_RAGGED_M, false, true, false, false, true>(mA, mB, mA, mB, p, bound, st);
         }
     }
     if (rc != GG_OK || !dX_tok) return rc;
