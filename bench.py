@@ -24,7 +24,7 @@ and the router's choices; every other tensor is computed in the step; FLOPs coun
 passes), padding rows not counted.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gg|reference]
-Prints ONE JSON line (rank 0).  Under torchrun every rank runs an independent
+Prints ONE JSON line (rank 0).  --only PASS times one GEMM pass alone (profiling aid).  Under torchrun every rank runs an independent
 replica of the layer on its own GPU (weak scaling, no collective on the data
 path); value = FLOPs of all ranks / max-over-ranks time.
 """
@@ -535,6 +535,75 @@ def run_gg(args, cfg):
         dist.destroy_process_group()
 
 
+def run_only(args, cfg):
+    """One GEMM pass of the step in isolation, on that pass's own operands only
+    (a few GB on the device): the case the profiler captures.  Operands that
+    the step computes are seeded random stand-ins of the same shape; the
+    routing is the config's.  Prints one diagnostic JSON line (not a bench
+    line)."""
+    import torch
+
+    import unpermute_route_hist_gb300 as gg
+    from unpermute_route_hist_gb300 import _lib, synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _lib.load()
+    T, k, E, K, N1, I, R = cfg.T, cfg.topk, cfg.E, cfg.K, cfg.N1, cfg.I, cfg.R
+    ids, _ = synth.route_choices(cfg)
+    r = gg.route_hist_offsets(torch.from_numpy(ids).to(dev), E)
+    m, gi = r["m_sizes"], r["gather_idx"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    bf = torch.bfloat16
+
+    def rnd(*shape):
+        return (torch.randn(*shape, device=dev, generator=gen) * 0.02).to(bf)
+
+    name = args.only
+    if name == "fwd1":
+        Xp, W1 = rnd(R, K), rnd(E, N1, K)
+        H, A2 = torch.empty(R, N1, dtype=bf, device=dev), torch.empty(R, I, dtype=bf, device=dev)
+        fn = lambda: gg.forward_swiglu(Xp, W1, m, gi, k, False, out=H, out_act=A2)
+    elif name == "fwd2":
+        A2, W2 = rnd(R, I), rnd(E, K, I)
+        Y2 = torch.empty(R, K, dtype=bf, device=dev)
+        fn = lambda: gg.forward(A2, W2, m, gi, None, k, False, True, False, out=Y2)
+    elif name == "dX2":
+        dYp, W2 = rnd(R, K), rnd(E, K, I)
+        dA2 = torch.empty(R, I, dtype=bf, device=dev)
+        fn = lambda: gg.backward_dX(dYp, W2, m, gi, T, k, False, False, out=dA2)
+    elif name == "dW2":
+        A2, dYp = rnd(R, I), rnd(R, K)
+        dW2 = torch.empty(E, K, I, dtype=bf, device=dev)
+        fn = lambda: gg.backward_dW(A2, dYp, m, gi, T, k, False, False, out=dW2)
+    elif name == "dX1":
+        dH, W1 = rnd(R, N1), rnd(E, N1, K)
+        dX1, dXt = torch.empty(R, K, dtype=bf, device=dev), torch.empty(T, K, dtype=bf, device=dev)
+        fn = lambda: gg.backward_dX(dH, W1, m, gi, T, k, True, False, token_sum=True, out=dX1,
+                                    out_tok=dXt)
+    elif name == "dW1":
+        Xp, dH = rnd(R, K), rnd(R, N1)
+        dW1 = torch.empty(E, N1, K, dtype=bf, device=dev)
+        fn = lambda: gg.backward_dW(Xp, dH, m, gi, T, k, False, False, out=dW1)
+    else:
+        raise SystemExit("unknown pass %r" % name)
+    flops = _gemm_passes(cfg)[name]
+    for _ in range(max(args.warmup, 1)):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / max(args.steps, 1)
+    print(json.dumps({"pass": name, "config": cfg.name, "ms": ms,
+                      "tflops": flops / (ms * 1e-3) / 1e12, "note": "diagnostic, not a bench line"}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -547,10 +616,14 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=640,
                     help="oracle rows per pass in the cpu_baseline sample (about 10 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["fwd1", "fwd2", "dX2", "dW2", "dX1", "dW1"],
+                    help="time one GEMM pass alone on its own operands (for profiling)")
     args = ap.parse_args()
     from unpermute_route_hist_gb300 import synth
     cfg = synth.CONFIGS[args.config]
-    if args.impl == "reference":
+    if args.only:
+        run_only(args, cfg)
+    elif args.impl == "reference":
         run_reference(args, cfg)
     else:
         run_gg(args, cfg)

@@ -362,6 +362,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
            | (static_cast<uint32_t>(M >> 4) << 24);       // M / 16
 }
 
+// ------------------------------------------------------------- L2 policy --
+
+// Cache policy that makes lines written with it the first candidates for
+// eviction from L2: for output streams that are not read again soon, so they
+// do not push out operand tiles that other CTAs are about to read.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_global_16_policy(void* ptr, const uint4& v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------- misc --
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

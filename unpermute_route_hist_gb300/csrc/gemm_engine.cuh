@@ -140,7 +140,9 @@ __device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
         const int e = lo;
         const int ut_e = s_tp[e + 1] - s_tp[e];
         const int loc = static_cast<int>(t - static_cast<int64_t>(s_tp[e]) * nt_total);
-        const int ngroups = (ut_e + kGroupU - 1) / kGroupU;
+        // group count rounded to nearest (at least 1): an expert a little taller
+        // than kGroupU units stays one group, so W[e] is streamed once
+        const int ngroups = max(1, (ut_e + kGroupU / 2) / kGroupU);
         const int gh = (ut_e + ngroups - 1) / ngroups;  // group height
         const int group = loc / (gh * nt_total);
         const int gsize = min(gh, ut_e - group * gh);
@@ -614,6 +616,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     } else if (warp < 6) {
         // ----------------------------------------------------- epilogue --
         const int q = warp & 3;        // TMEM lane quarter this warp may access
+        const uint64_t out_pol = l2_policy_evict_first();
         const int r = q * 32 + lane;   // tile row of this thread
         uint32_t acc_count = 0;
         for (int64_t t = slot; t < total_tiles; t += nslot) {
@@ -686,7 +689,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                             o.y = pack_bf16x2(__uint_as_float(v[pc * 8 + 2]) * sc, __uint_as_float(v[pc * 8 + 3]) * sc);
                             o.z = pack_bf16x2(__uint_as_float(v[pc * 8 + 4]) * sc, __uint_as_float(v[pc * 8 + 5]) * sc);
                             o.w = pack_bf16x2(__uint_as_float(v[pc * 8 + 6]) * sc, __uint_as_float(v[pc * 8 + 7]) * sc);
-                            *reinterpret_cast<uint4*>(orow + col) = o;
+                            st_global_16_policy(orow + col, o, out_pol);
                         }
                     }
                 }
@@ -707,7 +710,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                             o.y = pack_bf16x2(a[2], a[3]);
                             o.z = pack_bf16x2(a[4], a[5]);
                             o.w = pack_bf16x2(a[6], a[7]);
-                            *reinterpret_cast<uint4*>(arow_out + col0 / 2 + pc * 8) = o;
+                            st_global_16_policy(arow_out + col0 / 2 + pc * 8, o, out_pol);
                         }
                     }
                 }
