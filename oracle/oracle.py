@@ -218,6 +218,22 @@ def forward(X, W, m_sizes, gather_idx, topk_w, T, topk, permute_x, permute_y, fu
     return Y
 
 
+def forward_combine(X, W, m_sizes, gather_idx, topk_w, T, topk, permute_x):
+    """out [T, N] fp64: the forward with the weighted top-k combine fused
+    (matmul_ogs.py, the scatter path with several active experts per token:
+    token row t is the sum over its slots f = t*topk + j of w[f] * y_f).
+    Composed from the forward in token-slot order (scaled by w when given),
+    then a sum over each token's slots in ascending j."""
+    fm = 0 if topk_w is None else 1
+    Y = forward(X, W, m_sizes, gather_idx, topk_w, T, topk, permute_x, 1, fm)
+    N = Y.shape[1]
+    Y = Y.reshape(T, topk, N)
+    out = np.zeros((T, N), np.float64)
+    for j in range(topk):
+        out += Y[:, j, :]
+    return out
+
+
 def forward_rows(X, W, m_sizes, gather_idx, topk_w, topk, permute_x, permute_y, fuse_mul_post,
                  rows):
     """Expert-order rows computed one by one -> (values [n, N], destination rows [n])."""

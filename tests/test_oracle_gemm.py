@@ -65,6 +65,30 @@ def test_forward_integer_exact_all_flags(px, py, fm):
     np.testing.assert_array_equal(Y, _dense_expected_forward(X, W, r, topk, px, py, fm, w))
 
 
+@pytest.mark.parametrize("px,use_w", [(0, True), (1, True), (1, False)])
+def test_forward_combine_integer_exact(px, use_w):
+    """Fused combine: every token row is the (weighted) sum of its slots' rows,
+    checked against int64 products of every expert's full block."""
+    T, topk, E, K, N = 20, 3, 5, 16, 12
+    rng, ids, r = _setup(T, topk, E, K, N, 300 + px, empty=(2,))
+    X = _int_bf16(rng, (T if px else T * topk, K))
+    W = _int_bf16(rng, (E, N, K))
+    w = (rng.integers(1, 5, size=(T, topk)) / 4.0).astype(np.float32) if use_w else None
+    out = orc.forward_combine(X, W, r["m_sizes"], r["gather_idx"], w, T, topk, px)
+    slots = _dense_expected_forward(X, W, r, topk, px, 1, 1 if use_w else 0, w)
+    np.testing.assert_array_equal(out, slots.reshape(T, topk, N).sum(axis=1))
+
+
+def test_forward_combine_single_slot_is_scatter_forward():
+    T, topk, E, K, N = 40, 1, 4, 24, 16
+    rng, ids, r = _setup(T, topk, E, K, N, 17)
+    X = orc.round_bf16(rng.standard_normal((T, K)))
+    W = orc.round_bf16(rng.standard_normal((E, N, K)))
+    out = orc.forward_combine(X, W, r["m_sizes"], r["gather_idx"], None, T, topk, 1)
+    np.testing.assert_array_equal(out, orc.forward(X, W, r["m_sizes"], r["gather_idx"], None, T, topk,
+                                                   1, 1, 0))
+
+
 def test_forward_E1_identity_is_dense_matmul():
     rng = np.random.default_rng(1)
     R, K, N = 70, 48, 40
