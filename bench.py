@@ -465,6 +465,11 @@ def run_gg(args, cfg):
         "dW2_fused_slot_gather": (time_call(lambda: gg.backward_dW(
             A2, dY2, rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dW2,
             status=status)), passes["dW2"]),
+        # inference form of GEMM2 + combine: the combine fused into the epilogue
+        # (atomic adds; the per-slot rows the training step keeps are not stored)
+        "fwd2_fused_combine": (time_call(lambda: gg.forward_combine(
+            A2, W2, rr["m_sizes"], rr["gather_idx"], src["w"], k, False, out=out,
+            status=status)), passes["fwd2"]),
         "dW1_fused_token_gather": (time_call(lambda: gg.backward_dW(
             src["X"], dH, rr["m_sizes"], rr["gather_idx"], T, k, True, False, out=dW1,
             status=status), reps=1), passes["dW1"]),

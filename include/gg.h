@@ -183,6 +183,26 @@ int gg_forward(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
                int64_t N, int64_t K, int permute_x, int permute_y, int fuse_mul_post,
                gg_bf16* Y, int32_t* status, void* stream);
 
+/* ---------------------------------------------- forward + fused combine --
+ * The forward grouped GEMM with the weighted top-k combine of
+ * gg_unpermute_combine fused into its epilogue as atomic adds ([V] the
+ * scatter path: with several active experts per token each token row is a
+ * sum over its slots; the output starts zeroed):
+ *   out[t] = sum over the slots f = t*topk + j of  w[f] * (a_f @ W[e(f)]^T)
+ *   a_f, W[e] as gg_forward (permute_x selects X [T, K] with the gather, else
+ *   X [R, K] in expert order); w = topk_w [T, topk] fp32, or 1 when NULL.
+ *  out [T, N] bf16 out; the call zeroes it on the stream, then every slot's
+ *  row is added with bf16 atomic adds (each add rounded to bf16).
+ *  NOT deterministic: the order of a token's topk adds depends on scheduling,
+ *  so the last bits can differ from run to run; gg_forward with permute_y and
+ *  gg_unpermute_combine give the deterministic result (one fp32 sum, rounded
+ *  once).  The per-slot rows are not stored, so training that needs them
+ *  (the routing-weight gradient of gg_unpermute_combine_bwd) uses that path. */
+int gg_forward_combine(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
+                       const int32_t* gather_idx, const float* topk_w, int64_t T, int topk, int E,
+                       int64_t N, int64_t K, int permute_x, gg_bf16* out, int32_t* status,
+                       void* stream);
+
 /* ------------------------------------------------------ forward + SwiGLU --
  * The forward grouped GEMM with the gated activation fused into its epilogue
  * ([V] FusedActivation with reduction_n = 2: each pair of adjacent output

@@ -197,6 +197,34 @@ def test_mlp8_gemm1_swiglu_sampled():
                  magnitude=np.abs(orc.swiglu_bwd(Href, dA[dest])) * 4)
 
 
+def test_mlp8_gemm2_fused_combine_sampled():
+    """GEMM2 of mlp8 with the top-k combine fused into the epilogue (the
+    inference form), on sampled tokens: each token's slots are computed one by
+    one by the oracle and summed with the routing weights."""
+    cfg = synth.MLP8
+    T, k, E, K, I, R = cfg.T, cfg.topk, cfg.E, cfg.K, cfg.I, cfg.R
+    ids, w = synth.route_choices(cfg)
+    host = synth.moe_tensors(cfg, ("W2", "A2"))
+    st = status_tensor()
+    dev = torch.device("cuda:0")
+    r = gg.route_hist_offsets(torch.from_numpy(ids).to(dev), E, status=st)
+    out = gg.forward_combine(dbf(host["A2"]), dbf(host["W2"]), r["m_sizes"], r["gather_idx"], df32(w),
+                             k, False, status=st)
+    outh = hbf(out)
+    assert status_of(st) == 0
+    ro = orc.route(ids, T, k, E)
+    rng = np.random.default_rng(11)
+    toks = np.unique(np.concatenate([[0, T - 1], rng.integers(0, T, size=40)])).astype(np.int64)
+    slots = (toks[:, None] * k + np.arange(k)[None, :]).reshape(-1)
+    rows = ro["row_id_map"][slots].astype(np.int64)
+    vals, dest = orc.forward_rows(host["A2"], host["W2"], ro["m_sizes"], ro["gather_idx"], w, k, 0, 1, 1,
+                                  rows)
+    assert (dest == slots).all()
+    ref = vals.reshape(toks.size, k, K).sum(axis=1)
+    mag = np.abs(vals).reshape(toks.size, k, K).sum(axis=1)
+    assert_close(outh[toks], ref, "mlp8 GEMM2 fused combine", magnitude=(k + 1) / 4.0 * mag)
+
+
 def test_tiny_full():
     """The tiny workload end to end, every element (the oracle runs it in full)."""
     cfg = synth.TINY

@@ -242,6 +242,28 @@ def test_forward_swiglu(T, topk, E, K, N, px, store_y):
     assert_close(hbf(A), orc.swiglu(ref), "forward_swiglu act")
 
 
+@pytest.mark.parametrize("px,use_w", [(0, True), (1, True), (0, False)])
+@pytest.mark.parametrize("T,topk,E,K,N", [(200, 2, 5, 320, 264), (64, 2, 4, 128, 256), (513, 4, 9, 136, 520),
+                                          (97, 8, 16, 64, 1032)])
+def test_forward_combine(T, topk, E, K, N, px, use_w):
+    ids, w, ro = _problem(T, topk, E, K, N, (1,), 71 + T)
+    R = T * topk
+    X = synth.normal_bf16(21, "cx", (T if px else R, K), 0.1)
+    W = synth.normal_bf16(22, "cw", (E, N, K), 0.1)
+    wt = w if use_w else None
+    r = _route_gpu(ids, E)
+    st = status_tensor()
+    out = gg.forward_combine(dbf(X), dbf(W), r["m_sizes"], r["gather_idx"],
+                             None if wt is None else df32(wt), topk, bool(px), status=st)
+    assert status_of(st) == 0
+    ref = orc.forward_combine(X, W, ro["m_sizes"], ro["gather_idx"], wt, T, topk, px)
+    # each slot's row is rounded to bf16, then added with bf16 atomic adds (each
+    # add rounded): (topk + 1) roundings of at most 2^-9 of the slots' magnitude
+    slots = orc.forward(X, W, ro["m_sizes"], ro["gather_idx"], wt, T, topk, px, 1, 0 if wt is None else 1)
+    mag = np.abs(slots).reshape(T, topk, N).sum(axis=1)
+    assert_close(hbf(out), ref, "forward_combine", magnitude=(topk + 1) / 4.0 * mag)
+
+
 @pytest.mark.parametrize("rows,I", [(1, 8), (333, 64), (1000, 776)])
 def test_swiglu_bwd(rows, I):
     H = synth.normal_bf16(13, "sh", (rows, 2 * I), 1.0)

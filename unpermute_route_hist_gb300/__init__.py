@@ -5,10 +5,11 @@ package only loads it (``_lib``), marshals torch tensors into it (``api``)
 and provides seeded synthetic inputs (``synth``).
 """
 from . import api  # noqa: F401
-from .api import (backward_dW, backward_dX, dual_asym, forward, forward_swiglu, permute,  # noqa: F401
+from .api import (backward_dW, backward_dX, dual_asym, forward, forward_combine,  # noqa: F401
+                  forward_swiglu, permute,
                   route_hist_offsets, route_workspace_size, unpermute_combine,
                   swiglu_bwd, unpermute_combine_bwd)
 
 __all__ = ["route_hist_offsets", "route_workspace_size", "permute", "unpermute_combine", "forward",
            "backward_dX", "backward_dW", "dual_asym", "unpermute_combine_bwd",
-           "forward_swiglu", "swiglu_bwd"]
+           "forward_swiglu", "swiglu_bwd", "forward_combine"]

@@ -34,6 +34,8 @@ SIGNATURES = {
     "gg_unpermute_combine_bwd": (_int, [_vp, _vp, _vp, _vp, _i64, _int, _i64, _vp, _vp, _vp, _vp]),
     "gg_forward": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _int, _int,
                           _vp, _vp, _vp]),
+    "gg_forward_combine": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _vp,
+                                  _vp, _vp]),
     "gg_forward_swiglu": (_int, [_vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _vp, _vp,
                                  _vp, _vp]),
     "gg_swiglu_bwd": (_int, [_vp, _vp, _i64, _i64, _vp, _vp]),

@@ -140,6 +140,28 @@ def forward(X, W, m_sizes, gather_idx, topk_w, topk: int, permute_x=False, permu
     return Y
 
 
+def forward_combine(X, W, m_sizes, gather_idx, topk_w, topk: int, permute_x=False, *, out=None,
+                    status=None):
+    """out [T, N]: forward with the weighted top-k combine fused (atomic adds,
+    not bit-deterministic); topk_w [T, topk] fp32 or None (unit weights)."""
+    _need(X, torch.bfloat16, "X")
+    _need(W, torch.bfloat16, "W")
+    E, N, K = W.shape
+    _need(m_sizes, torch.int32, "m_sizes", (E,))
+    rows = X.shape[0]
+    T = rows if permute_x else rows // topk
+    R = T * topk
+    if not permute_x and rows != R:
+        raise ValueError("X must have T*topk rows without permute_x")
+    _need(gather_idx, torch.int32, "gather_idx", (R,))
+    _opt(topk_w, torch.float32, "topk_w")
+    out = _out(out, (T, N), torch.bfloat16, X.device, "out")
+    rc = _lib.load().gg_forward_combine(_p(X), _p(W), _p(m_sizes), _p(gather_idx), _p(topk_w), T, topk,
+                                        E, N, K, int(permute_x), _p(out), _p(status), _stream(X.device))
+    _lib.check("gg_forward_combine", rc)
+    return out
+
+
 def forward_swiglu(X, W, m_sizes, gather_idx, topk: int, permute_x=False, *, store_y=True, out=None,
                    out_act=None, status=None):
     """(Y [R, N] or None, A [R, N/2]): forward with the SwiGLU of interleaved gate/up columns."""

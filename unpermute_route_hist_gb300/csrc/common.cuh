@@ -378,6 +378,14 @@ __device__ __forceinline__ void st_global_16_policy(void* ptr, const uint4& v, u
                  : "memory");
 }
 
+// out[0..7] += v (eight bf16 lanes, each add rounded to bf16), one atomic
+// reduction per 16 bytes; the order of concurrent adds is unspecified.
+__device__ __forceinline__ void red_add_bf16x8(void* ptr, const uint4& v) {
+    asm volatile("red.global.add.noftz.v4.bf16x2 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------- misc --
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

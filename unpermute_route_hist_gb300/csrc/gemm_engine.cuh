@@ -82,6 +82,9 @@ struct GemmParams {
     int64_t ld_out;
     int scatter_out;         // RAGGED_M: store row gather_idx[i] instead of i
     const float* scale;      // RAGGED_M: multiply row i by scale[gather_idx[i]]
+    // RAGGED_M: add row i (scaled) into token row gather_idx[i] / topk of a
+    // zeroed [T, N] output with bf16 atomic adds (the top-k combine, fused)
+    int combine_out;
     // RAGGED_M: also (or only, when out is null) store the gated activation of
     // each pair of adjacent output columns, act[c] = silu(y[2c]) * y[2c+1]
     uint16_t* act_out;
@@ -633,11 +636,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 if (KIND == KIND_RAGGED_M) {
                     const int64_t i = ti.row0 + r;
                     dest = i;
-                    if (p.scatter_out || p.scale) {
+                    if (p.scatter_out || p.scale || p.combine_out) {
                         const int32_t f = p.gather_idx[i];
                         if (f < 0 || f >= p.R) { set_status(p.status, GG_DEV_BAD_ROW_INDEX); dest = -1; }
                         else {
                             if (p.scatter_out) dest = f;
+                            if (p.combine_out) dest = static_cast<int64_t>(static_cast<uint32_t>(f) / static_cast<uint32_t>(p.topk));
                             if (p.scale) sc = p.scale[f];
                         }
                     }
@@ -689,7 +693,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                             o.y = pack_bf16x2(__uint_as_float(v[pc * 8 + 2]) * sc, __uint_as_float(v[pc * 8 + 3]) * sc);
                             o.z = pack_bf16x2(__uint_as_float(v[pc * 8 + 4]) * sc, __uint_as_float(v[pc * 8 + 5]) * sc);
                             o.w = pack_bf16x2(__uint_as_float(v[pc * 8 + 6]) * sc, __uint_as_float(v[pc * 8 + 7]) * sc);
-                            st_global_16_policy(orow + col, o, out_pol);
+                            if (KIND == KIND_RAGGED_M && p.combine_out) red_add_bf16x8(orow + col, o);
+                            else st_global_16_policy(orow + col, o, out_pol);
                         }
                     }
                 }

@@ -1,6 +1,7 @@
 // gemm_ragged_m.cu -- entry points whose output rows are ragged per expert:
 // the forward grouped GEMM (also with the fused SwiGLU of matmul_ogs.py's
-// FusedActivation) and the backward dX (interface.py, grouped_gemm_forward
+// FusedActivation, or with the top-k combine fused into the epilogue as
+// atomic adds) and the backward dX (interface.py, grouped_gemm_forward
 // and grouped_gemm_dX).  Both run the persistent tcgen05
 // engine of gemm_engine.cuh over the expert-order row tiles.
 #include "gemm_engine.cuh"
@@ -104,6 +105,42 @@ int gg_forward_swiglu(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes
     p.ld_out = N;
     p.act_out = A;
     p.ld_act = N / 2;
+    CUtensorMap mA{}, mB{};
+    const int64_t bound = row_tile_bound(R, E) * ((N + kBN - 1) / kBN);
+    if (permute_x) {
+        if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN)) return GG_ERR_CUDA;
+        p.ga = GatherSrc{X, K, T, K, ROW_TOKEN};
+        return launch_gemm<KIND_RAGGED_M, false, false, true, false, false>(mB, mB, mB, mB, p, bound, st);
+    }
+    if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN / 2)) return GG_ERR_CUDA;
+    if (!encode_map_2d(&mA, X, K, R, K, kBK, kBM)) return GG_ERR_CUDA;
+    return launch_gemm<KIND_RAGGED_M, false, false, false, false, true>(mA, mB, mA, mB, p, bound, st);
+}
+
+int gg_forward_combine(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
+                       const int32_t* gather_idx, const float* topk_w, int64_t T, int topk, int E,
+                       int64_t N, int64_t K, int permute_x, gg_bf16* out, int32_t* status,
+                       void* stream) {
+    if (T < 0 || topk < 1 || E < 1 || N < 0 || K < 0) return GG_ERR_INVALID_ARG;
+    if (topk > GG_MAX_TOPK || E > GG_MAX_EXPERTS || N % 8 || K % 8) return GG_ERR_UNSUPPORTED;
+    const int64_t R = T * topk;
+    if (R >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+        return GG_ERR_UNSUPPORTED;
+    if (T == 0 || N == 0) return GG_OK;
+    if (!X || !W || !m_sizes || !gather_idx || !out) return GG_ERR_INVALID_ARG;
+    if (!al16(X) || !al16(W) || !al16(out)) return GG_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the adds accumulate into a zeroed output (every token row gets topk adds)
+    cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(T * N) * 2, st);
+    if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+    if (K == 0) return GG_OK;
+    GemmParams p = base_params(E, topk, R, m_sizes, gather_idx, status);
+    p.N = static_cast<int>(N);
+    p.Kred = static_cast<int>(K);
+    p.out = out;
+    p.ld_out = N;
+    p.combine_out = 1;
+    p.scale = topk_w;
     CUtensorMap mA{}, mB{};
     const int64_t bound = row_tile_bound(R, E) * ((N + kBN - 1) / kBN);
     if (permute_x) {
