@@ -312,6 +312,22 @@ void oracle_swiglu_bwd(const uint16_t* H, const uint16_t* dA, int64_t rows, int6
         }
 }
 
+/* The same gradient with the upstream dA given exactly (fp64) instead of as
+ * stored bf16 values: the form the dX pass reaches when the activation's
+ * backward runs on its unrounded output. */
+void oracle_swiglu_bwd_f64(const uint16_t* H, const double* dA, int64_t rows, int64_t I,
+                           double* dH) {
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < I; ++c) {
+            double g = bf16_to_double(H[r * 2 * I + 2 * c]);
+            double u = bf16_to_double(H[r * 2 * I + 2 * c + 1]);
+            double d = dA[r * I + c];
+            double s = 1.0 / (1.0 + exp(-g));
+            dH[r * 2 * I + 2 * c] = d * u * s * (1.0 + g * (1.0 - s));
+            dH[r * 2 * I + 2 * c + 1] = d * g * s;
+        }
+}
+
 /* ------------------------------------------------------------ backward dX -- */
 
 /* One row of dX ([U] grouped_gemm_dX): reduce over N,

@@ -63,6 +63,7 @@ def _load():
                                                     _vp]),
             "oracle_swiglu": (None, [_f64p, _i64, _i64, _f64p]),
             "oracle_swiglu_bwd": (None, [_u16p, _u16p, _i64, _i64, _f64p]),
+            "oracle_swiglu_bwd_f64": (None, [_u16p, _f64p, _i64, _i64, _f64p]),
             "oracle_forward": (None, [_u16p, _u16p, _i32p, _vp, _vp, _i64, _int, _int, _i64, _i64,
                                       _int, _int, _int, _f64p]),
             "oracle_forward_rows": (None, [_u16p, _u16p, _i32p, _vp, _vp, _int, _int, _i64, _i64,
@@ -203,6 +204,17 @@ def swiglu_bwd(H, dA) -> np.ndarray:
     return dH
 
 
+def swiglu_bwd_f64(H, dA) -> np.ndarray:
+    """dH [rows, 2I] fp64 from stored H (bf16) and an exact upstream dA (fp64)."""
+    H = _c(H, np.uint16)
+    dA = _c(dA, np.float64)
+    rows, two_i = H.shape
+    assert dA.shape == (rows, two_i // 2)
+    dH = np.empty((rows, two_i), np.float64)
+    _load().oracle_swiglu_bwd_f64(H, dA, rows, two_i // 2, dH)
+    return dH
+
+
 # ----------------------------------------------------------- grouped GEMMs --
 
 def forward(X, W, m_sizes, gather_idx, topk_w, T, topk, permute_x, permute_y, fuse_mul_post):
@@ -261,6 +273,13 @@ def backward_dX(dY, W, m_sizes, gather_idx, T, topk, permute_x, permute_y):
     _load().oracle_backward_dX(dY, W, m, _ptr(g), T, topk, E, N, K, int(permute_x),
                                int(permute_y), dX)
     return dX
+
+
+def backward_dX_swiglu(dY, W, m_sizes, gather_idx, T, topk, permute_y, H):
+    """dH [R, 2K] fp64: the dX pass (expert-order rows, no scatter) followed by
+    the SwiGLU backward on its unrounded output dA [R, K] with the stored H."""
+    dA = backward_dX(dY, W, m_sizes, gather_idx, T, topk, 0, permute_y)
+    return swiglu_bwd_f64(H, dA)
 
 
 def backward_dX_rows(dY, W, m_sizes, gather_idx, permute_x, permute_y, rows):

@@ -258,3 +258,36 @@ def test_swiglu_bwd_matches_autograd():
     act = torch.nn.functional.silu(Ht[:, 0::2]) * Ht[:, 1::2]
     (act * torch.from_numpy(orc.widen_bf16(dA))).sum().backward()
     np.testing.assert_allclose(dH, Ht.grad.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_swiglu_bwd_f64_agrees_with_stored_bf16_form():
+    """With an upstream gradient that is exactly representable in bf16 the
+    fp64-input form gives the stored-input form's values bit for bit."""
+    rng = np.random.default_rng(21)
+    rows, I = 17, 24
+    H = orc.round_bf16(rng.standard_normal((rows, 2 * I)) * 2)
+    dA = orc.round_bf16(rng.standard_normal((rows, I)))
+    np.testing.assert_array_equal(orc.swiglu_bwd_f64(H, orc.widen_bf16(dA)), orc.swiglu_bwd(H, dA))
+
+
+@pytest.mark.parametrize("py", [0, 1])
+def test_backward_dX_swiglu_matches_autograd(py):
+    """dX followed by the SwiGLU backward, against torch autograd (CPU, fp64)
+    through the dense per-expert product and the activation."""
+    T, topk, E, K, N = 18, 2, 4, 16, 12
+    rng, ids, r = _setup(T, topk, E, K, N, 40 + py, empty=(1,))
+    R = T * topk
+    dY = orc.round_bf16(rng.standard_normal((R, N)))
+    W = orc.round_bf16(rng.standard_normal((E, N, K)))
+    H = orc.round_bf16(rng.standard_normal((R, 2 * K)) * 2)
+    dH = orc.backward_dX_swiglu(dY, W, r["m_sizes"], r["gather_idx"], T, topk, py, H)
+    g = r["gather_idx"]
+    expert = np.searchsorted(r["offsets"], np.arange(R), side="right") - 1
+    dYt = torch.from_numpy(orc.widen_bf16(dY))
+    Wt = torch.from_numpy(orc.widen_bf16(W))
+    rows_dy = dYt[torch.from_numpy(g.astype(np.int64))] if py else dYt
+    dA = torch.stack([rows_dy[i] @ Wt[expert[i]] for i in range(R)])
+    Ht = torch.from_numpy(orc.widen_bf16(H)).requires_grad_(True)
+    act = torch.nn.functional.silu(Ht[:, 0::2]) * Ht[:, 1::2]
+    (act * dA).sum().backward()
+    np.testing.assert_allclose(dH, Ht.grad.numpy(), rtol=1e-11, atol=1e-11)
