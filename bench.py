@@ -470,6 +470,10 @@ def run_gg(args, cfg):
         "fwd2_fused_combine": (time_call(lambda: gg.forward_combine(
             A2, W2, rr["m_sizes"], rr["gather_idx"], src["w"], k, False, out=out,
             status=status)), passes["fwd2"]),
+        # dX2 with the SwiGLU backward fused into its epilogue (no dA buffer); the
+        # step runs dX2 then gg_swiglu_bwd, which measures faster
+        "dX2_fused_swiglu_bwd": (time_call(lambda: gg.backward_dX_swiglu(
+            dYp, W2, rr["m_sizes"], k, H, out=dH, status=status)), passes["dX2"]),
         "dW1_fused_token_gather": (time_call(lambda: gg.backward_dW(
             src["X"], dH, rr["m_sizes"], rr["gather_idx"], T, k, True, False, out=dW1,
             status=status), reps=1), passes["dW1"]),

@@ -239,6 +239,23 @@ int gg_backward_dX(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes,
                    int permute_x, int permute_y, gg_bf16* dX, gg_bf16* dX_tok, int32_t* status,
                    void* stream);
 
+/* ---------------------------------------------- backward dX + SwiGLU bwd --
+ * The backward dX of a grouped GEMM whose input was the SwiGLU activation of
+ * gg_forward_swiglu, with the activation's backward fused into the epilogue
+ * (the two steps of gg_backward_dX and gg_swiglu_bwd in one pass; the
+ * activation gradient never goes to memory and is not rounded to bf16):
+ *   for every expert-order row i of expert e:
+ *     da = dY[i] @ W[e]                                  (fp32, [K])
+ *     g = H[i, 2c], u = H[i, 2c+1], s = 1 / (1 + exp(-g))
+ *     dH[i, 2c]   = bf16( da[c] * u * s * (1 + g * (1 - s)) )
+ *     dH[i, 2c+1] = bf16( da[c] * g * s )
+ *  dY [R, N] bf16 in expert order (gg_permute a token-slot-order gradient
+ *  first); W [E, N, K]; H [R, 2K] bf16, the stored forward output of
+ *  gg_forward_swiglu (expert order); dH [R, 2K] bf16 out. */
+int gg_backward_dX_swiglu(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes, int64_t T,
+                          int topk, int E, int64_t N, int64_t K, const gg_bf16* H, gg_bf16* dH,
+                          int32_t* status, void* stream);
+
 /* ------------------------------------------------------------ backward dW --
  * Gradient of the expert weights ([U] grouped_gemm_dW; [V] ragged-dw comment:
  * the reduction dimension is each expert's own rows):

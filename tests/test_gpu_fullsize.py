@@ -225,6 +225,28 @@ def test_mlp8_gemm2_fused_combine_sampled():
     assert_close(outh[toks], ref, "mlp8 GEMM2 fused combine", magnitude=(k + 1) / 4.0 * mag)
 
 
+def test_mlp8_dX2_swiglu_sampled():
+    """dX of mlp8's GEMM2 with the SwiGLU backward fused (the benchmark's
+    form), on sampled expert-order rows."""
+    cfg = synth.MLP8
+    T, k, E, K, I, N1, R = cfg.T, cfg.topk, cfg.E, cfg.K, cfg.I, cfg.N1, cfg.R
+    ids, w = synth.route_choices(cfg)
+    host = synth.moe_tensors(cfg, ("W2",))
+    dYp = synth.normal_bf16(6, "mlp8/dYp", (R, K), 0.02)
+    H = synth.normal_bf16(7, "mlp8/H", (R, N1), 1.0)
+    st = status_tensor()
+    dev = torch.device("cuda:0")
+    r = gg.route_hist_offsets(torch.from_numpy(ids).to(dev), E, status=st)
+    dH = gg.backward_dX_swiglu(dbf(dYp), dbf(host["W2"]), r["m_sizes"], k, dbf(H), status=st)
+    dHh = hbf(dH)
+    assert status_of(st) == 0
+    ro = orc.route(ids, T, k, E)
+    rows = _sample_rows(ro["offsets"], np.random.default_rng(8), n_random=24)
+    dA, dest = orc.backward_dX_rows(dYp, host["W2"], ro["m_sizes"], ro["gather_idx"], 0, 0, rows)
+    assert (dest == rows).all()
+    assert_close(dHh[rows], orc.swiglu_bwd_f64(H[rows], dA), "mlp8 dX2 + SwiGLU bwd")
+
+
 def test_tiny_full():
     """The tiny workload end to end, every element (the oracle runs it in full)."""
     cfg = synth.TINY

@@ -264,6 +264,24 @@ def test_forward_combine(T, topk, E, K, N, px, use_w):
     assert_close(hbf(out), ref, "forward_combine", magnitude=(topk + 1) / 4.0 * mag)
 
 
+@pytest.mark.parametrize("T,topk,E,K,N", [(200, 2, 5, 264, 320), (64, 2, 4, 128, 256), (513, 4, 9, 520, 136),
+                                          (33, 1, 3, 8, 64)])
+def test_backward_dX_swiglu(T, topk, E, K, N):
+    """dX on the SwiGLU output with the activation's backward fused (K = the
+    activation width; H and dH are [R, 2K])."""
+    ids, w, ro = _problem(T, topk, E, K, N, (2,), 81 + T)
+    R = T * topk
+    dY = synth.normal_bf16(31, "bdy", (R, N), 0.1)
+    W = synth.normal_bf16(32, "bw", (E, N, K), 0.1)
+    H = synth.normal_bf16(33, "bh", (R, 2 * K), 1.0)
+    r = _route_gpu(ids, E)
+    st = status_tensor()
+    dH = gg.backward_dX_swiglu(dbf(dY), dbf(W), r["m_sizes"], topk, dbf(H), status=st)
+    assert status_of(st) == 0
+    ref = orc.backward_dX_swiglu(dY, W, ro["m_sizes"], ro["gather_idx"], T, topk, 0, H)
+    assert_close(hbf(dH), ref, "backward_dX_swiglu")
+
+
 @pytest.mark.parametrize("rows,I", [(1, 8), (333, 64), (1000, 776)])
 def test_swiglu_bwd(rows, I):
     H = synth.normal_bf16(13, "sh", (rows, 2 * I), 1.0)

@@ -41,6 +41,8 @@ SIGNATURES = {
     "gg_swiglu_bwd": (_int, [_vp, _vp, _i64, _i64, _vp, _vp]),
     "gg_backward_dX": (_int, [_vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _int, _vp, _vp,
                               _vp, _vp]),
+    "gg_backward_dX_swiglu": (_int, [_vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _vp, _vp, _vp,
+                                     _vp]),
     "gg_backward_dW": (_int, [_vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _int, _vp, _vp,
                               _vp]),
     "gg_dual_asym": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _int, _int,

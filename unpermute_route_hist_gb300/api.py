@@ -209,6 +209,25 @@ def backward_dX(dY, W, m_sizes, gather_idx, T: int, topk: int, permute_x=False, 
     return (dX, dXt) if token_sum else dX
 
 
+def backward_dX_swiglu(dY, W, m_sizes, topk: int, H, *, out=None, status=None):
+    """dH [R, 2K]: dX of the GEMM on the SwiGLU output (dY in expert order),
+    with the SwiGLU backward on the stored H fused into the epilogue."""
+    _need(dY, torch.bfloat16, "dY")
+    _need(W, torch.bfloat16, "W")
+    E, N, K = W.shape
+    _need(m_sizes, torch.int32, "m_sizes", (E,))
+    R = dY.shape[0]
+    if R % topk:
+        raise ValueError("dY must have T*topk rows")
+    _need(dY, torch.bfloat16, "dY", (R, N))
+    _need(H, torch.bfloat16, "H", (R, 2 * K))
+    dH = _out(out, (R, 2 * K), torch.bfloat16, dY.device, "out")
+    rc = _lib.load().gg_backward_dX_swiglu(_p(dY), _p(W), _p(m_sizes), R // topk, topk, E, N, K, _p(H),
+                                           _p(dH), _p(status), _stream(dY.device))
+    _lib.check("gg_backward_dX_swiglu", rc)
+    return dH
+
+
 def backward_dW(X, dY, m_sizes, gather_idx, T: int, topk: int, permute_x=False, permute_y=False,
                 *, out=None, status=None):
     _need(X, torch.bfloat16, "X")

@@ -85,6 +85,11 @@ struct GemmParams {
     // RAGGED_M: add row i (scaled) into token row gather_idx[i] / topk of a
     // zeroed [T, N] output with bf16 atomic adds (the top-k combine, fused)
     int combine_out;
+    // RAGGED_M: the output is the upstream gradient dA of a SwiGLU over
+    // interleaved gate/up columns; instead of dA, store dH[i, 2c], dH[i, 2c+1]
+    // into out (ld_out = 2N) from the stored pre-activation H[i, 2c], H[i, 2c+1]
+    const uint16_t* swiglu_h;
+    int64_t ld_h;
     // RAGGED_M: also (or only, when out is null) store the gated activation of
     // each pair of adjacent output columns, act[c] = silu(y[2c]) * y[2c+1]
     uint16_t* act_out;
@@ -720,6 +725,66 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     }
                 }
             };
+            // (dense operands only: the 10-warp gather kernels have no registers to spare)
+            if constexpr (KIND == KIND_RAGGED_M && !Tr::kAnyGather) if (p.swiglu_h) {
+                // SwiGLU backward on the fp32 accumulator (dA), 16 columns a step;
+                // each 8-H group gives 4 (gate, up) gradient pairs.  The H rows of
+                // this CTA's next tile are prefetched into L2 now (that epilogue
+                // runs a whole main loop later), and each step's 32 H values are
+                // loaded one step ahead, so the stores do not wait on DRAM.
+                {
+                    const int64_t tn = t + nslot;
+                    if (tn < total_tiles) {
+                        const TileInfo tni = decode_tile<KIND, PAIR>(tn, p, s_off, s_tp, rank);
+                        if (r < tni.rows) {
+                            const char* hn = reinterpret_cast<const char*>(p.swiglu_h + (tni.row0 + r) * p.ld_h + 2 * tni.n0);
+                            const int nbytes = 4 * min(kBN, ncols - tni.n0);  // 2 H values per column
+                            for (int b = 0; b < nbytes; b += 128) prefetch_l2(hn + b);
+                        }
+                    }
+                }
+                const uint16_t* hrow = orow ? p.swiglu_h + dest * p.ld_h : nullptr;
+                auto load_h = [&](int col0, uint4 (&h)[4]) {
+                    if (hrow) {
+#pragma unroll
+                        for (int qd = 0; qd < 4; ++qd)
+                            if (col0 + qd * 4 < ncols)
+                                h[qd] = __ldg(reinterpret_cast<const uint4*>(hrow + 2 * col0 + qd * 8));
+                    }
+                };
+                uint4 hv[4], hnext[4];
+                load_h(ti.n0, hv);
+#pragma unroll 1
+                for (int c = 0; c < kBN / 16; ++c) {
+                    const int col0 = ti.n0 + c * 16;
+                    if (c + 1 < kBN / 16) load_h(col0 + 16, hnext);
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(taddr0 + c * 16, v);
+                    tmem_ld_wait();
+                    if (c == kBN / 16 - 1) release_acc();
+                    if (hrow) {
+#pragma unroll
+                        for (int qd = 0; qd < 4; ++qd) {
+                            if (col0 + qd * 4 < ncols) {
+                                const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&hv[qd]);
+                                uint32_t o[4];
+#pragma unroll
+                                for (int a = 0; a < 4; ++a) {
+                                    const float2 gu = __bfloat1622float2(hh[a]);  // (gate, up)
+                                    const float d = __uint_as_float(v[qd * 4 + a]);
+                                    const float sg = 1.0f / (1.0f + __expf(-gu.x));
+                                    o[a] = pack_bf16x2(d * gu.y * sg * (1.0f + gu.x * (1.0f - sg)), d * gu.x * sg);
+                                }
+                                st_global_16_policy(orow + 2 * col0 + qd * 8, make_uint4(o[0], o[1], o[2], o[3]), out_pol);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int qd = 0; qd < 4; ++qd) hv[qd] = hnext[qd];
+                }
+                ++acc_count;
+                continue;
+            }
             // Four 32-column TMEM loads per wait: the loads' latency is paid once per
             // 128 columns.  The accumulator is handed back to the MMA warp as soon as
             // the last load has landed in registers, before its columns are stored.

@@ -2,7 +2,7 @@
 // the forward grouped GEMM (also with the fused SwiGLU of matmul_ogs.py's
 // FusedActivation, or with the top-k combine fused into the epilogue as
 // atomic adds) and the backward dX (interface.py, grouped_gemm_forward
-// and grouped_gemm_dX).  Both run the persistent tcgen05
+// and grouped_gemm_dX), also with the SwiGLU backward fused into its epilogue.  Both run the persistent tcgen05
 // engine of gemm_engine.cuh over the expert-order row tiles.
 #include "gemm_engine.cuh"
 
@@ -193,6 +193,37 @@ int gg_backward_dX(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes,
     }
     if (rc != GG_OK || !dX_tok) return rc;
     return combine_launch(dX, nullptr, nullptr, T, topk, K, dX_tok, status, st);
+}
+
+int gg_backward_dX_swiglu(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes, int64_t T,
+                          int topk, int E, int64_t N, int64_t K, const gg_bf16* H, gg_bf16* dH,
+                          int32_t* status, void* stream) {
+    if (T < 0 || topk < 1 || E < 1 || N < 0 || K < 0) return GG_ERR_INVALID_ARG;
+    if (topk > GG_MAX_TOPK || E > GG_MAX_EXPERTS || N % 8 || K % 8) return GG_ERR_UNSUPPORTED;
+    const int64_t R = T * topk;
+    if (R >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || 2 * K >= (int64_t(1) << 31))
+        return GG_ERR_UNSUPPORTED;
+    if (R == 0 || K == 0) return GG_OK;
+    if (!dY || !W || !m_sizes || !H || !dH) return GG_ERR_INVALID_ARG;
+    if (!al16(dY) || !al16(W) || !al16(H) || !al16(dH)) return GG_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 0) {  // dA = 0, so dH = 0
+        const cudaError_t e = cudaMemsetAsync(dH, 0, static_cast<size_t>(R * 2 * K) * 2, st);
+        if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+        return GG_OK;
+    }
+    GemmParams p = base_params(E, topk, R, m_sizes, nullptr, status);
+    p.N = static_cast<int>(K);
+    p.Kred = static_cast<int>(N);
+    p.out = dH;
+    p.ld_out = 2 * K;
+    p.swiglu_h = H;
+    p.ld_h = 2 * K;
+    CUtensorMap mA{}, mB{};
+    if (!encode_map_3d(&mB, W, K, N, E, K, N * K, 64, kBK)) return GG_ERR_CUDA;
+    const int64_t bound = row_tile_bound(R, E) * ((K + kBN - 1) / kBN);
+    if (!encode_map_2d(&mA, dY, N, R, N, kBK, kBM)) return GG_ERR_CUDA;
+    return launch_gemm<KIND_RAGGED_M, false, true, false, false, true>(mA, mB, mA, mB, p, bound, st);
 }
 
 }  // extern "C"
