@@ -24,7 +24,8 @@ and the router's choices; every other tensor is computed in the step; FLOPs coun
 passes), padding rows not counted.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gg|reference]
-Prints ONE JSON line (rank 0).  --only PASS times one GEMM pass alone (profiling aid).  Under torchrun every rank runs an independent
+Prints ONE JSON line (rank 0).  --only PASS times one GEMM pass alone (profiling aid);
+--suite times the other workloads (fine128, zipf64, the dual GEMM and its sweep).  Under torchrun every rank runs an independent
 replica of the layer on its own GPU (weak scaling, no collective on the data
 path); value = FLOPs of all ranks / max-over-ranks time.
 """
@@ -613,6 +614,115 @@ def run_only(args, cfg):
           flush=True)
 
 
+def run_suite(args):
+    """Diagnostic timings of the workloads the benchmark step does not cover:
+    the GEMM passes of fine128 (E=128, top-8, empty and near-empty experts) and
+    zipf64 (skewed routing), the dual GEMM at its stated shape and over a
+    sweep of (m0, m1).  Operands that the step would compute are seeded random
+    stand-ins; routing is each config's.  One JSON line per workload."""
+    import torch
+
+    import unpermute_route_hist_gb300 as gg
+    from unpermute_route_hist_gb300 import _lib, synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _lib.load()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    bf = torch.bfloat16
+    peaks, src_kind = _peaks()
+    tflops_sus = _peak_value(peaks, ["bf16_tflops_sustained", "bf16_tflops"], 1700.0)
+
+    def rnd(*shape, std=0.02):
+        return (torch.randn(*shape, device=dev, generator=gen) * std).to(bf)
+
+    def timed(fn, reps=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    for cfg in (synth.FINE128, synth.ZIPF64):
+        T, k, E, K, N1, I, R = cfg.T, cfg.topk, cfg.E, cfg.K, cfg.N1, cfg.I, cfg.R
+        ids, _ = synth.route_choices(cfg)
+        r = gg.route_hist_offsets(torch.from_numpy(ids).to(dev), E)
+        m, gi = r["m_sizes"], r["gather_idx"]
+        hist = m.cpu().numpy()
+        Xp, W1, dH = rnd(R, K), rnd(E, N1, K), rnd(R, N1)
+        H = torch.empty(R, N1, dtype=bf, device=dev)
+        passes = {
+            "fwd1": (lambda: gg.forward(Xp, W1, m, gi, None, k, False, False, False, out=H), 2.0 * R * N1 * K),
+            "dX1": (lambda: gg.backward_dX(dH, W1, m, gi, T, k, True, False, token_sum=True), 2.0 * R * N1 * K),
+            "dW1": (lambda: gg.backward_dW(Xp, dH, m, gi, T, k, False, False), 2.0 * R * N1 * K),
+        }
+        res = {}
+        for name, (fn, fl) in passes.items():
+            ms = timed(fn)
+            res[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}
+        del Xp, W1, dH, H
+        if I:
+            A2, W2, dYp = rnd(R, I), rnd(E, K, I), rnd(R, K)
+            fl = 2.0 * R * K * I
+            for name, fn in (("fwd2", lambda: gg.forward(A2, W2, m, gi, None, k, False, True, False)),
+                             ("dX2", lambda: gg.backward_dX(dYp, W2, m, gi, T, k, False, False)),
+                             ("dW2", lambda: gg.backward_dW(A2, dYp, m, gi, T, k, False, False))):
+                ms = timed(fn)
+                res[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}
+            del A2, W2, dYp
+        tot_ms = sum(v["ms"] for v in res.values())
+        tot_fl = 3.0 * (2.0 * R * N1 * K + (2.0 * R * K * I if I else 0.0))
+        print(json.dumps({"suite": cfg.name, "passes": res, "gemm_tflops": tot_fl / (tot_ms * 1e-3) / 1e12,
+                          "frac_of_sustained_peak": tot_fl / (tot_ms * 1e-3) / 1e12 / tflops_sus,
+                          "peak_source": src_kind, "experts_empty": int((hist == 0).sum()),
+                          "largest_expert_share": float(hist.max() / hist.sum())}), flush=True)
+        torch.cuda.empty_cache()
+
+    # Dual GEMM: per call as issued from Python (host-bound for small shapes), and
+    # the device time of the same calls replayed from a captured CUDA graph.
+    def graph_ms(fn, reps=20):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    sweep = {}
+    ms_list = [128, 256, 512, 1024, 2048, 4096, 8192]
+    kd, n0, n1 = synth.DUAL.k, synth.DUAL.n0, synth.DUAL.n1
+    W0, W1 = rnd(kd, n0, std=kd ** -0.5), rnd(kd, n1, std=kd ** -0.5)
+    for m0 in ms_list:
+        for m1 in ms_list:
+            X0, X1 = rnd(m0, kd, std=kd ** -0.5), rnd(m1, kd, std=kd ** -0.5)
+            Y0 = torch.empty(m0, n0, dtype=bf, device=dev)
+            Y1 = torch.empty(m1, n1, dtype=bf, device=dev)
+            fn = lambda: gg.dual_asym(X0, X1, W0, W1, out0=Y0, out1=Y1)
+            ms = timed(fn)
+            gms = graph_ms(fn)
+            fl = 2.0 * kd * (m0 * n0 + m1 * n1)
+            sweep["%d,%d" % (m0, m1)] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                                         "graph_ms": gms, "graph_tflops": fl / (gms * 1e-3) / 1e12}
+    base = sweep["%d,%d" % (synth.DUAL.m0, synth.DUAL.m1)]
+    print(json.dumps({"suite": "dual", "stated_shape": base, "sweep_m0_m1": sweep,
+                      "largest_graph_tflops": max(v["graph_tflops"] for v in sweep.values())}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -627,10 +737,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["fwd1", "fwd2", "dX2", "dW2", "dX1", "dW1"],
                     help="time one GEMM pass alone on its own operands (for profiling)")
+    ap.add_argument("--suite", action="store_true",
+                    help="time fine128, zipf64 and the dual GEMM (diagnostic lines, not the bench line)")
     args = ap.parse_args()
     from unpermute_route_hist_gb300 import synth
     cfg = synth.CONFIGS[args.config]
-    if args.only:
+    if args.suite:
+        run_suite(args)
+    elif args.only:
         run_only(args, cfg)
     elif args.impl == "reference":
         run_reference(args, cfg)

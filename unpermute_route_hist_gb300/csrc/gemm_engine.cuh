@@ -35,6 +35,8 @@
 // hand (kmajor_chunk_offset, and chunk c of an MN row r at c ^ (r & 7)).
 #pragma once
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace gg {
@@ -972,9 +974,19 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
     using Tr = GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>;
     auto kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>;
     const size_t smem = gemm_smem_bytes<PAIR>(p.E);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(gemm_smem_bytes<PAIR>(GG_MAX_EXPERTS)));
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+    if (dev < 0 || dev >= 64) dev = 0;
+    // the shared-memory opt-in is set once per kernel and device (host overhead
+    // matters for small launches)
+    static std::atomic<bool> smem_set[64];
+    if (!smem_set[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(gemm_smem_bytes<PAIR>(GG_MAX_EXPERTS)));
+        if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+        smem_set[dev].store(true, std::memory_order_release);
+    }
     const int64_t sms = num_sms();
     if (tile_bound < 1) tile_bound = 1;
     if (!PAIR) {
@@ -995,9 +1007,6 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
         // as many 2-CTA clusters as can be resident at once (a GPC with an odd
         // SM count leaves an SM out), at most one per tile pair
         static int max_clusters[64] = {0};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev < 0 || dev >= 64) dev = 0;
         if (max_clusters[dev] == 0) {
             cfg.gridDim = dim3(static_cast<unsigned>(sms & ~int64_t(1)));
             int n = 0;
