@@ -14,8 +14,9 @@
 //                     gets the token's output gradient times the slot weight,
 //                     and each weight gets <output gradient, forward row>.
 //
-// Both move whole rows as 16-byte vectors (row widths are multiples of 8
-// bf16), one CTA per row in a grid that is a multiple of the SM count.
+// They move whole rows as 16-byte vectors (row widths are multiples of 8
+// bf16): permute and combine one warp per token row, the combine backward one
+// CTA per token row, in grids of at most 8 CTAs per SM.
 #include "common.cuh"
 
 namespace gg {
@@ -31,27 +32,61 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     return v;
 }
 
+constexpr int kWarpsPerCta = kMoveThreads / 32;
+constexpr int kVecsInFlight = 4;  // 16-byte loads each lane keeps in flight
+
+// Slot j's entry of a per-token index held two per lane (j = lane, lane + 32);
+// a full-warp shuffle, so every lane must call it with the same j.
+__device__ __forceinline__ int32_t slot_entry(int32_t lo, int32_t hi, int j) {
+    const int32_t a = __shfl_sync(0xffffffffu, lo, j & 31);
+    const int32_t b = __shfl_sync(0xffffffffu, hi, j & 31);
+    return j < 32 ? a : b;
+}
+__device__ __forceinline__ float slot_entry_f(float lo, float hi, int j) {
+    const float a = __shfl_sync(0xffffffffu, lo, j & 31);
+    const float b = __shfl_sync(0xffffffffu, hi, j & 31);
+    return j < 32 ? a : b;
+}
+
+// Row index of slot f through the map (identity when NULL); -1 and a status
+// code when it is out of range.
+__device__ __forceinline__ int32_t mapped_row(const int32_t* map, int64_t f, int64_t R, int32_t* status) {
+    int32_t r = map ? map[f] : static_cast<int32_t>(f);
+    if (r < 0 || r >= R) {
+        set_status(status, GG_DEV_BAD_ROW_INDEX);
+        r = -1;
+    }
+    return r;
+}
+
+// One warp per token: its topk destination rows are held in lanes, the row is
+// read in passes of 32 lanes x kVecsInFlight 16-byte vectors (all loads of a
+// pass in flight together), and each pass is written to every destination.
 __global__ void __launch_bounds__(kMoveThreads)
 permute_kernel(const uint4* __restrict__ X, const int32_t* __restrict__ row_id_map, int64_t T,
                int topk, int64_t row_vecs, uint4* __restrict__ Xp, int64_t R, int32_t* status) {
-    __shared__ int32_t dst_s[GG_MAX_TOPK];
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        __syncthreads();
-        if (threadIdx.x < topk) {
-            int32_t d = row_id_map[t * topk + threadIdx.x];
-            if (d < 0 || d >= R) {
-                set_status(status, GG_DEV_BAD_ROW_INDEX);
-                d = -1;
-            }
-            dst_s[threadIdx.x] = d;
-        }
-        __syncthreads();
+    const int lane = lane_id();
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerCta;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + warp_id(); t < T; t += nwarps) {
+        const int32_t d_lo = lane < topk ? mapped_row(row_id_map, t * topk + lane, R, status) : -1;
+        const int32_t d_hi = lane + 32 < topk ? mapped_row(row_id_map, t * topk + lane + 32, R, status) : -1;
         const uint4* src = X + t * row_vecs;
-        for (int64_t c = threadIdx.x; c < row_vecs; c += kMoveThreads) {
-            const uint4 v = ld_stream(src + c);
+        for (int64_t c0 = 0; c0 < row_vecs; c0 += 32 * kVecsInFlight) {
+            uint4 v[kVecsInFlight];
+#pragma unroll
+            for (int u = 0; u < kVecsInFlight; ++u) {
+                const int64_t c = c0 + u * 32 + lane;
+                if (c < row_vecs) v[u] = ld_stream(src + c);
+            }
             for (int j = 0; j < topk; ++j) {
-                const int32_t d = dst_s[j];
-                if (d >= 0) Xp[static_cast<int64_t>(d) * row_vecs + c] = v;
+                const int32_t d = slot_entry(d_lo, d_hi, j);
+                if (d < 0) continue;
+                uint4* dst = Xp + static_cast<int64_t>(d) * row_vecs;
+#pragma unroll
+                for (int u = 0; u < kVecsInFlight; ++u) {
+                    const int64_t c = c0 + u * 32 + lane;
+                    if (c < row_vecs) dst[c] = v[u];
+                }
             }
         }
     }
@@ -67,37 +102,53 @@ __device__ __forceinline__ void bf16x8_fma(float (&acc)[8], const uint4& v, floa
     }
 }
 
+// One warp per token: out[t] = sum over slots j (in order) of w_j * Y[row_j],
+// fp32, one rounding; passes of 32 lanes x kVecsInFlight vectors, the loads of
+// one slot's pass in flight together.
 __global__ void __launch_bounds__(kMoveThreads)
 combine_kernel(const uint4* __restrict__ Y, const int32_t* __restrict__ row_id_map,
                const float* __restrict__ topk_w, int64_t T, int topk, int64_t row_vecs, int64_t R,
                uint4* __restrict__ out, int32_t* status) {
-    __shared__ int32_t src_s[GG_MAX_TOPK];
-    __shared__ float w_s[GG_MAX_TOPK];
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        __syncthreads();
-        if (threadIdx.x < topk) {
-            const int64_t f = t * topk + threadIdx.x;
-            int32_t s = row_id_map ? row_id_map[f] : static_cast<int32_t>(f);
-            if (s < 0 || s >= R) {
-                set_status(status, GG_DEV_BAD_ROW_INDEX);
-                s = -1;
-            }
-            src_s[threadIdx.x] = s;
-            w_s[threadIdx.x] = topk_w ? topk_w[f] : 1.0f;
-        }
-        __syncthreads();
-        for (int64_t c = threadIdx.x; c < row_vecs; c += kMoveThreads) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const int lane = lane_id();
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerCta;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + warp_id(); t < T; t += nwarps) {
+        const int32_t s_lo = lane < topk ? mapped_row(row_id_map, t * topk + lane, R, status) : -1;
+        const int32_t s_hi = lane + 32 < topk ? mapped_row(row_id_map, t * topk + lane + 32, R, status) : -1;
+        const float w_lo = lane < topk ? (topk_w ? topk_w[t * topk + lane] : 1.0f) : 0.0f;
+        const float w_hi = lane + 32 < topk ? (topk_w ? topk_w[t * topk + lane + 32] : 1.0f) : 0.0f;
+        for (int64_t c0 = 0; c0 < row_vecs; c0 += 32 * kVecsInFlight) {
+            float acc[kVecsInFlight][8];
+#pragma unroll
+            for (int u = 0; u < kVecsInFlight; ++u)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[u][q] = 0.f;
             for (int j = 0; j < topk; ++j) {
-                const int32_t s = src_s[j];
-                if (s >= 0) bf16x8_fma(acc, ld_stream(Y + static_cast<int64_t>(s) * row_vecs + c), w_s[j]);
+                const int32_t sr = slot_entry(s_lo, s_hi, j);
+                const float w = slot_entry_f(w_lo, w_hi, j);
+                if (sr < 0) continue;
+                const uint4* src = Y + static_cast<int64_t>(sr) * row_vecs;
+                uint4 v[kVecsInFlight];
+#pragma unroll
+                for (int u = 0; u < kVecsInFlight; ++u) {
+                    const int64_t c = c0 + u * 32 + lane;
+                    if (c < row_vecs) v[u] = ld_stream(src + c);
+                }
+#pragma unroll
+                for (int u = 0; u < kVecsInFlight; ++u)
+                    if (c0 + u * 32 + lane < row_vecs) bf16x8_fma(acc[u], v[u], w);
             }
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            out[t * row_vecs + c] = o;
+#pragma unroll
+            for (int u = 0; u < kVecsInFlight; ++u) {
+                const int64_t c = c0 + u * 32 + lane;
+                if (c < row_vecs) {
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+                    o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+                    o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+                    o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+                    out[t * row_vecs + c] = o;
+                }
+            }
         }
     }
 }
@@ -220,7 +271,7 @@ unsigned move_grid(int64_t rows) {
 int permute_launch(const uint16_t* X, const int32_t* row_id_map, int64_t T, int topk, int64_t K,
                    uint16_t* Xp, int32_t* status, cudaStream_t stream) {
     const int64_t R = T * topk;
-    permute_kernel<<<move_grid(T), kMoveThreads, 0, stream>>>(
+    permute_kernel<<<move_grid((T + kWarpsPerCta - 1) / kWarpsPerCta), kMoveThreads, 0, stream>>>(
         reinterpret_cast<const uint4*>(X), row_id_map, T, topk, K / 8, reinterpret_cast<uint4*>(Xp),
         R, status);
     return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
@@ -251,7 +302,7 @@ int combine_bwd_launch(const uint16_t* G, const uint16_t* Y, const int32_t* row_
 int combine_launch(const uint16_t* Y, const int32_t* row_id_map, const float* topk_w, int64_t T,
                    int topk, int64_t N, uint16_t* out, int32_t* status, cudaStream_t stream) {
     const int64_t R = T * topk;
-    combine_kernel<<<move_grid(T), kMoveThreads, 0, stream>>>(
+    combine_kernel<<<move_grid((T + kWarpsPerCta - 1) / kWarpsPerCta), kMoveThreads, 0, stream>>>(
         reinterpret_cast<const uint4*>(Y), row_id_map, topk_w, T, topk, N / 8, R,
         reinterpret_cast<uint4*>(out), status);
     return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
