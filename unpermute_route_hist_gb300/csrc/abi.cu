@@ -65,7 +65,7 @@ static bool encode(CUtensorMap* m, uint32_t rank, const void* base, const cuuint
         snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled unavailable");
         return false;
     }
-    const cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     // The swizzle span equals the box's inner extent (rows of 64 or 128 bytes),
     // which is the layout the MMA descriptors expect for that tile.
     const CUtensorMapSwizzle sw = box[0] * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
@@ -95,6 +95,32 @@ bool encode_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, u
     const cuuint64_t strides[2] = {stride1_elems * 2, stride2_elems * 2};
     const cuuint32_t box[3] = {b0, b1, 1};
     return encode(m, 3, base, dims, strides, box);
+}
+
+// An MN-major operand [rows, cols] (cols contiguous, a multiple of 64) viewed
+// as 3-D {64, rows, cols / 64}: the third dimension steps 128 bytes along a
+// row, so one box {64, box_rows, box_chunks} brings box_chunks adjacent
+// 64-column chunks of box_rows rows, chunk after chunk, in one copy.
+bool encode_map_mn_chunks(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                          uint64_t row_stride_elems, uint32_t box_rows, uint32_t box_chunks) {
+    if (cols % 64) return false;
+    const cuuint64_t dims[3] = {64, rows, cols / 64};
+    const cuuint64_t strides[2] = {row_stride_elems * 2, 128};
+    const cuuint32_t box[3] = {64, box_rows, box_chunks};
+    return encode(m, 3, base, dims, strides, box);
+}
+
+// The same view per plane of a 3-D tensor [planes, rows, cols] (the expert
+// weights): {64, rows, cols / 64, planes}, box {64, box_rows, box_chunks, 1}.
+bool encode_map_mn_chunks_planes(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                                 uint64_t planes, uint64_t row_stride_elems,
+                                 uint64_t plane_stride_elems, uint32_t box_rows,
+                                 uint32_t box_chunks) {
+    if (cols % 64) return false;
+    const cuuint64_t dims[4] = {64, rows, cols / 64, planes};
+    const cuuint64_t strides[3] = {row_stride_elems * 2, 128, plane_stride_elems * 2};
+    const cuuint32_t box[4] = {64, box_rows, box_chunks, 1};
+    return encode(m, 4, base, dims, strides, box);
 }
 
 }  // namespace gg

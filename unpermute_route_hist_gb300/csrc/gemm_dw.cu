@@ -56,5 +56,12 @@ extern "C" int gg_backward_dW(const gg_bf16* X, const gg_bf16* dY, const int32_t
         return launch_gemm<KIND_RAGGED_K, true, true, true, false, false>(mA, mB, mA, mB, p, bound, st);
     if (permute_x)
         return launch_gemm<KIND_RAGGED_K, true, true, false, true, false>(mA, mB, mA, mB, p, bound, st);
+    // both dense: when the widths allow, read each operand's stage as one box of
+    // 64-column chunks (one TMA copy per operand and stage, not two)
+    if (N % 64 == 0 && K % 64 == 0) {
+        if (!encode_map_mn_chunks(&mA, dY, N, R, N, kBK, kBM / 64)) return GG_ERR_CUDA;
+        if (!encode_map_mn_chunks(&mB, X, K, R, K, kBK, (kBN / 2) / 64)) return GG_ERR_CUDA;
+        p.mn_chunk_view = 1;
+    }
     return launch_gemm<KIND_RAGGED_K, true, true, false, false, true>(mA, mB, mA, mB, p, bound, st);
 }

@@ -92,6 +92,10 @@ struct GemmParams {
     // into out (ld_out = 2N) from the stored pre-activation H[i, 2c], H[i, 2c+1]
     const uint16_t* swiglu_h;
     int64_t ld_h;
+    // pair, dense: the MN-major maps are 64-column chunk views (one box per
+    // operand and stage instead of one per chunk); RAGGED_K: A and B,
+    // RAGGED_M: B, a view per expert plane
+    int mn_chunk_view;
     // RAGGED_M: also (or only, when out is null) store the gated activation of
     // each pair of adjacent output columns, act[c] = silu(y[2c]) * y[2c+1]
     uint16_t* act_out;
@@ -437,8 +441,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                             bar = mapa_u32(&ctl->full[stage], 0);
                         }
                         const int32_t nb = ti.n0 + static_cast<int32_t>(rank) * (kBN / 2);
+                        const bool chunk_view = KIND != KIND_DUAL && p.mn_chunk_view;
                         if (!A_MN) {
                             tma_load_2d_pair(sA, mA, bar, red, static_cast<int32_t>(ti.row0));
+                        } else if (chunk_view) {
+                            tma_load_3d_pair(sA, mA, bar, 0, red, static_cast<int32_t>(ti.row0 / 64));
                         } else {
 #pragma unroll
                             for (int cc = 0; cc < kBM / 64; ++cc)
@@ -447,6 +454,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         if (!B_MN) {
                             if (KIND == KIND_RAGGED_M) tma_load_3d_pair(sB, mB, bar, red, nb, ti.e);
                             else tma_load_2d_pair(sB, mB, bar, red, nb);
+                        } else if (chunk_view) {
+                            if (KIND == KIND_RAGGED_M) tma_load_4d_pair(sB, mB, bar, 0, red, nb / 64, ti.e);
+                            else tma_load_3d_pair(sB, mB, bar, 0, red, nb / 64);
                         } else {
 #pragma unroll
                             for (int cc = 0; cc < Tr::kBRows / 64; ++cc) {
@@ -965,6 +975,12 @@ bool encode_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
                    uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_outer);
 bool encode_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                    uint64_t stride1_elems, uint64_t stride2_elems, uint32_t b0, uint32_t b1);
+bool encode_map_mn_chunks(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                          uint64_t row_stride_elems, uint32_t box_rows, uint32_t box_chunks);
+bool encode_map_mn_chunks_planes(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                                 uint64_t planes, uint64_t row_stride_elems,
+                                 uint64_t plane_stride_elems, uint32_t box_rows,
+                                 uint32_t box_chunks);
 int num_sms();
 void record_cuda_error(cudaError_t e);
 

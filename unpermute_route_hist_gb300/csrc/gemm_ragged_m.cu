@@ -188,6 +188,11 @@ int gg_backward_dX(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes,
             rc = launch_gemm<KIND_RAGGED_M, false, true, true, false, false>(mB, mB, mB, mB, p, bound, st);
         } else {
             if (!encode_map_2d(&mA, dY, N, R, N, kBK, kBM)) return GG_ERR_CUDA;
+            if (K % 64 == 0) {  // W's 128-column half tile as one box of two 64-column chunks
+                if (!encode_map_mn_chunks_planes(&mB, W, K, N, E, K, N * K, kBK, (kBN / 2) / 64))
+                    return GG_ERR_CUDA;
+                p.mn_chunk_view = 1;
+            }
             rc = launch_gemm<KIND_RAGGED_M, false, true, false, false, true>(mA, mB, mA, mB, p, bound, st);
         }
     }
@@ -223,6 +228,10 @@ int gg_backward_dX_swiglu(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_
     if (!encode_map_3d(&mB, W, K, N, E, K, N * K, 64, kBK)) return GG_ERR_CUDA;
     const int64_t bound = row_tile_bound(R, E) * ((K + kBN - 1) / kBN);
     if (!encode_map_2d(&mA, dY, N, R, N, kBK, kBM)) return GG_ERR_CUDA;
+    if (K % 64 == 0) {
+        if (!encode_map_mn_chunks_planes(&mB, W, K, N, E, K, N * K, kBK, (kBN / 2) / 64)) return GG_ERR_CUDA;
+        p.mn_chunk_view = 1;
+    }
     return launch_gemm<KIND_RAGGED_M, false, true, false, false, true>(mA, mB, mA, mB, p, bound, st);
 }
 
