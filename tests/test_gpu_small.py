@@ -144,6 +144,65 @@ def test_unpermute_combine_bwd(T, topk, N, use_map, use_w, want_dw):
         assert dw is None
 
 
+@pytest.mark.parametrize("T,topk,E,K", [(40, 64, 5, 64), (33, 33, 70, 136), (17, 64, 2048, 8)])
+def test_movers_max_topk(T, topk, E, K):
+    """topk at its maximum (64) and past one warp's width (33): route, permute,
+    combine and combine backward against the oracle."""
+    ids = _ids(T, topk, E, 91 + topk)
+    R = T * topk
+    r = _route_gpu(ids, E, pad_block=16)
+    ro = orc.route(ids, T, topk, E, pad_block=16)
+    for k in ("m_sizes", "offsets", "padded_offsets", "gather_idx", "row_id_map"):
+        np.testing.assert_array_equal(r[k].cpu().numpy(), ro[k], err_msg=k)
+    X = synth.normal_bf16(41, "mx", (T, K), 1.0)
+    st = status_tensor()
+    Xp = gg.permute(dbf(X), r["row_id_map"], topk, status=st)
+    np.testing.assert_array_equal(hbf(Xp), orc.permute(X, ro["gather_idx"], topk))
+    rng = np.random.default_rng(topk)
+    w = (rng.random((T, topk)) / topk).astype(np.float32)
+    Y = synth.normal_bf16(42, "my", (R, K), 0.25)
+    out = gg.unpermute_combine(dbf(Y), r["row_id_map"], df32(w), T, topk, status=st)
+    assert_close(hbf(out), orc.unpermute_combine(Y, ro["row_id_map"], w, T, topk), "combine topk=%d" % topk)
+    G = synth.normal_bf16(43, "mg", (T, K), 0.25)
+    dY, dw = gg.unpermute_combine_bwd(dbf(G), dbf(Y), r["row_id_map"], df32(w), T, topk, status=st)
+    rdY, rdw = orc.unpermute_combine_bwd(G, Y, ro["row_id_map"], w, T, topk)
+    assert_close(hbf(dY), rdY, "combine bwd dY topk=%d" % topk)
+    got = dw.cpu().numpy().astype(np.float64)
+    assert np.abs(got - rdw).max() <= 1e-4 * (float(np.sqrt(np.mean(rdw * rdw))) + 1e-30) + 1e-6
+    assert status_of(st) == 0
+
+
+def test_gemms_max_experts():
+    """E at its maximum (2048): most experts empty or one row; forward, dX and
+    dW on the dense 2-CTA path, and the fused combine with topk = 64."""
+    T, topk, E, K, N = 300, 4, 2048, 64, 128
+    ids, w, ro = _problem(T, topk, E, K, N, (), 5)
+    R = T * topk
+    X = synth.normal_bf16(51, "ex", (R, K), 0.1)
+    W = synth.normal_bf16(52, "ew", (E, N, K), 0.1)
+    dY = synth.normal_bf16(53, "edy", (R, N), 0.1)
+    r = _route_gpu(ids, E)
+    st = status_tensor()
+    Y = gg.forward(dbf(X), dbf(W), r["m_sizes"], r["gather_idx"], None, topk, status=st)
+    assert_close(hbf(Y), orc.forward(X, W, ro["m_sizes"], ro["gather_idx"], None, T, topk, 0, 0, 0), "fwd E=2048")
+    dX = gg.backward_dX(dbf(dY), dbf(W), r["m_sizes"], r["gather_idx"], T, topk, status=st)
+    assert_close(hbf(dX), orc.backward_dX(dY, W, ro["m_sizes"], ro["gather_idx"], T, topk, 0, 0), "dX E=2048")
+    dW = gg.backward_dW(dbf(X), dbf(dY), r["m_sizes"], r["gather_idx"], T, topk, status=st)
+    assert_close(hbf(dW), orc.backward_dW(X, dY, ro["m_sizes"], ro["gather_idx"], T, topk, 0, 0), "dW E=2048")
+    assert status_of(st) == 0
+    T2, k2 = 24, 64
+    ids2, w2, ro2 = _problem(T2, k2, 300, K, N, (), 6)
+    X2 = synth.normal_bf16(54, "ex2", (T2, K), 0.1)
+    W2 = synth.normal_bf16(55, "ew2", (300, N, K), 0.1)
+    r2 = _route_gpu(ids2, 300)
+    out = gg.forward_combine(dbf(X2), dbf(W2), r2["m_sizes"], r2["gather_idx"], df32(w2), k2, True, status=st)
+    ref = orc.forward_combine(X2, W2, ro2["m_sizes"], ro2["gather_idx"], w2, T2, k2, 1)
+    slots = orc.forward(X2, W2, ro2["m_sizes"], ro2["gather_idx"], w2, T2, k2, 1, 1, 1)
+    mag = np.abs(slots).reshape(T2, k2, N).sum(axis=1)
+    assert_close(hbf(out), ref, "forward_combine topk=64", magnitude=(k2 + 1) / 4.0 * mag)
+    assert status_of(st) == 0
+
+
 # ---------------------------------------------------------- grouped GEMMs --
 
 SHAPES = [
