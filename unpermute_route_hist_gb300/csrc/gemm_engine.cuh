@@ -237,6 +237,7 @@ struct GemmTraits {
     static_assert(!(PAIR && (A_GATHER || B_GATHER)), "2-CTA tiles are loaded by TMA only");
     static_assert(!(PAIR && KIND == KIND_DUAL), "the dual GEMM runs on single CTAs");
     static constexpr bool kAnyGather = A_GATHER || B_GATHER;
+    static constexpr bool kCpGatherFence = kAnyGather;  // cp.async-written stages
     static constexpr int kThreads = 32 * (6 + (kAnyGather ? kGatherWarps : 0));
     static constexpr int kStages = PAIR ? 6 : 4;
     static constexpr int kBRows = PAIR ? kBN / 2 : kBN;  // B tile rows (n) held by one CTA
@@ -541,45 +542,101 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             }
             fence_proxy_async_smem();
         };
-        if (!PAIR || leader) {
-            // ----------------------------------------------- MMA issuer --
+        if ((!PAIR || leader) && KIND != KIND_RAGGED_K) {
+            // ------------------------------------ MMA issuer (lane 0 alone) --
+            // No stage needs the warp (no ragged tails to zero), so lane 0 runs
+            // the loop by itself: no per-stage shuffle or warp barrier between
+            // one stage's MMAs and the next.
+            if (lane == 0) {
+                int stage = 0;
+                uint32_t phase = 0;
+                uint32_t acc_count = 0;
+                bool ok = true, any_mma = false;
+                for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
+                    const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
+                    if (ti.nkb == 0) continue;
+                    const uint32_t buf = acc_count & 1u;
+                    const uint32_t acc_phase = (acc_count >> 1) & 1u;
+                    if (!mbar_wait(&ctl->tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.status, 0, kWaitLimitNs, PAIR)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + buf * kBN;
+                    for (int kb = 0; kb < ti.nkb; ++kb) {
+                        if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+                        tc_fence_after();
+                        // cp.async writes are generic-proxy; order them before the
+                        // tensor core's async-proxy reads of this stage
+                        if (Tr::kCpGatherFence) fence_proxy_async_smem();
+                        const uint32_t sA = stage0 + stage * kStageBytes;
+                        const uint32_t sB = sA + kABytes;
+#pragma unroll
+                        for (int ks = 0; ks < kBK / 16; ++ks) {
+                            const uint64_t ad = operand_desc<A_MN>(sA, ks), bd = operand_desc<B_MN>(sB, ks);
+                            const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
+                            if (PAIR) umma_bf16_pair(d_tmem, ad, bd, Tr::kIdesc, acc);
+                            else umma_bf16(d_tmem, ad, bd, Tr::kIdesc, acc);
+                        }
+                        if (PAIR) umma_commit_pair(&ctl->empty[stage], 0x3);
+                        else umma_commit(&ctl->empty[stage]);
+                        any_mma = true;
+                        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    }
+                    if (!ok) break;
+                    if (PAIR) umma_commit_pair(&ctl->tmem_full[buf], 0x3);
+                    else umma_commit(&ctl->tmem_full[buf]);
+                    ++acc_count;
+                }
+                // All MMAs of this thread finish before TMEM is released.
+                if (any_mma) {
+                    if (PAIR) umma_commit_pair(&ctl->drain, 0x1);
+                    else umma_commit(&ctl->drain);
+                    int dummy = 0;
+                    mbar_wait(&ctl->drain, 0, reinterpret_cast<volatile int*>(&dummy), p.status);
+                }
+            }
+            __syncwarp();
+        } else if (!PAIR || leader) {
+            // ------------------------- MMA issuer with ragged tails (dW) --
+            // Lane 0 waits and issues; the other lanes join it only at a tail
+            // stage, to zero the rows past the expert's end.  Every lane walks the
+            // same loop (no early exit), so the warp-wide steps at tail stages
+            // always match up, also after lane 0 has given up on a wait.
             int stage = 0;
             uint32_t phase = 0;
             uint32_t pfull_par = 0;  // per-slot parity of pfull (tail stages only)
             uint32_t acc_count = 0;
             bool ok = true, any_mma = false;
-            for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
+            for (int64_t t = slot; t < total_tiles; t += nslot) {
                 const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
                 if (ti.nkb == 0) continue;
                 const uint32_t buf = acc_count & 1u;
                 const uint32_t acc_phase = (acc_count >> 1) & 1u;
-                if (!warp_wait(&ctl->tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.status, 0, PAIR)) { ok = false; break; }
-                tc_fence_after();
+                if (lane == 0 && ok) {
+                    ok = mbar_wait(&ctl->tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.status, 0, kWaitLimitNs, PAIR);
+                    tc_fence_after();
+                }
                 const uint32_t d_tmem = tmem_base + buf * kBN;
                 for (int kb = 0; kb < ti.nkb; ++kb) {
-                    if (!warp_wait(&ctl->full[stage], phase, abort_flag, p.status)) { ok = false; break; }
-                    tc_fence_after();
+                    if (lane == 0 && ok) ok = mbar_wait(&ctl->full[stage], phase, abort_flag, p.status);
                     const uint32_t sA = stage0 + stage * kStageBytes;
                     const uint32_t sB = sA + kABytes;
                     int ksteps = kBK / 16;
-                    if (KIND == KIND_RAGGED_K) {
-                        const int valid = min(kBK, ti.red_len - kb * kBK);
-                        if (valid < kBK) {
-                            ksteps = (valid + 15) / 16;
-                            zero_tail(stage, valid, ksteps * 16);
-                            __syncwarp();
-                            if (Tr::kTailFwd) {
-                                // the odd CTA's half of this stage has landed, tail zeroed
-                                if (!warp_wait(&ctl->pfull[stage], (pfull_par >> stage) & 1u, abort_flag, p.status, 0, true)) {
-                                    ok = false;
-                                    break;
-                                }
-                                pfull_par ^= 1u << stage;
-                                tc_fence_after();
-                            }
+                    const int valid = KIND == KIND_RAGGED_K ? min(kBK, ti.red_len - kb * kBK) : kBK;
+                    if (valid < kBK) {  // the same for every lane
+                        ksteps = (valid + 15) / 16;
+                        // lane 0 has seen the stage land (or given up)
+                        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) zero_tail(stage, valid, ksteps * 16);
+                        __syncwarp();
+                        if (Tr::kTailFwd && lane == 0) {
+                            // the odd CTA's half of this stage has landed, tail zeroed
+                            if (ok) ok = mbar_wait(&ctl->pfull[stage], (pfull_par >> stage) & 1u, abort_flag, p.status, 0, kWaitLimitNs, true);
+                            pfull_par ^= 1u << stage;
                         }
                     }
-                    if (lane == 0) {
+                    if (lane == 0 && ok) {
+                        tc_fence_after();
                         // cp.async writes are generic-proxy; order them before the
                         // tensor core's async-proxy reads of this stage
                         if (Tr::kAnyGather) fence_proxy_async_smem();
@@ -593,15 +650,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         else umma_commit(&ctl->empty[stage]);
                         any_mma = true;
                     }
-                    __syncwarp();
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
-                if (!ok) break;
-                if (lane == 0) {
+                if (lane == 0 && ok) {
                     if (PAIR) umma_commit_pair(&ctl->tmem_full[buf], 0x3);
                     else umma_commit(&ctl->tmem_full[buf]);
                 }
-                __syncwarp();
                 ++acc_count;
             }
             // All MMAs of this thread finish before TMEM is released.
