@@ -251,14 +251,20 @@ struct GemmTraits {
     // own tail rows before the MMA, so the odd CTA's copies complete on its own
     // barrier and the odd CTA then signals the even one (pfull).
     static constexpr bool kTailFwd = PAIR && KIND == KIND_RAGGED_K;
+    // pair kernels with ragged rows stage each epilogue warp's rows in shared memory
+    // (4 KB a warp) so that global stores go out as whole 128-byte row segments (dW's
+    // tiles, long reductions sharing shared-memory bandwidth, measured faster without)
+    static constexpr bool kEpiStage = PAIR && KIND == KIND_RAGGED_M;
     static_assert(kStages <= kMaxStages, "stage ring");
 };
+
+constexpr int kEpiStageBytes = 4 * 4096;  // 4 epilogue warps x 32 rows x 128 B
 
 template <bool PAIR>
 __host__ __device__ constexpr size_t gemm_smem_bytes(int E) {
     return 1024 /* alignment slack */ +
            static_cast<size_t>(PAIR ? 6 : 4) * (kABytes + (PAIR ? kBN / 2 : kBN) * kBK * 2) +
-           sizeof(SharedCtl) + 2 * static_cast<size_t>(E + 1) * sizeof(int32_t) + 16;
+           (PAIR ? kEpiStageBytes : 0) + sizeof(SharedCtl) + 2 * static_cast<size_t>(E + 1) * sizeof(int32_t) + 16;
 }
 static_assert(gemm_smem_bytes<true>(GG_MAX_EXPERTS) <= 227 * 1024, "shared memory (pair)");
 static_assert(gemm_smem_bytes<false>(GG_MAX_EXPERTS) <= 227 * 1024, "shared memory");
@@ -299,7 +305,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     uint8_t* stage_base = smem;
     constexpr int kStages = Tr::kStages;
     constexpr uint32_t kStageBytes = Tr::kStageBytes;
-    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kStages * kStageBytes);
+    uint8_t* epi_stage = smem + kStages * kStageBytes;  // kEpiStageBytes when Tr::kEpiStage
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(epi_stage + (Tr::kEpiStage ? kEpiStageBytes : 0));
     int32_t* s_off = reinterpret_cast<int32_t*>(ctl + 1);
     int32_t* s_tp = s_off + (p.E + 1);
 
@@ -752,8 +759,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 continue;
             }
             const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN;
-            // convert and store 32 accumulator columns starting at output column col0
-            auto store_chunk = [&](const uint32_t (&v)[32], int col0) {
+            // convert and store 32 accumulator columns starting at output column col0,
+            // straight from registers (16 bytes of the thread's own row per store)
+            auto store_out32 = [&](const uint32_t (&v)[32], int col0) {
                 if (orow) {
 #pragma unroll
                     for (int pc = 0; pc < 4; ++pc) {
@@ -769,6 +777,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         }
                     }
                 }
+            };
+            auto store_act32 = [&](const uint32_t (&v)[32], int col0) {
                 if (arow_out) {
                     // 16 gate/up pairs of this chunk -> 16 activations (two 16-byte pieces)
 #pragma unroll
@@ -790,6 +800,50 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         }
                     }
                 }
+            };
+            // Staged store of 64 columns (va: col0.., vb: col0+32..): every lane writes
+            // its row's 128 bytes to the warp's staging rows (16-byte pieces rotated by
+            // row, so neither phase has bank conflicts), then eight lanes per row write
+            // four whole 128-byte row segments per store instruction.  Every lane of
+            // the warp takes part (shuffles and warp barriers).
+            const bool staged = Tr::kEpiStage && out != nullptr;
+            uint8_t* stg = epi_stage + q * 4096;
+            uint16_t* drow[8];
+            if (staged) {
+                const uint64_t mine = reinterpret_cast<uint64_t>(orow);
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int src = (lane >> 3) + 4 * it;
+                    const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(mine), src);
+                    const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(mine >> 32), src);
+                    drow[it] = reinterpret_cast<uint16_t*>((static_cast<uint64_t>(hi) << 32) | lo);
+                }
+            }
+            auto store_out64_staged = [&](const uint32_t (&va)[32], const uint32_t (&vb)[32], int col0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t* v = j < 4 ? va : vb;
+                    const int b = (j & 3) * 8;
+                    uint4 o;
+                    o.x = pack_bf16x2(__uint_as_float(v[b + 0]) * sc, __uint_as_float(v[b + 1]) * sc);
+                    o.y = pack_bf16x2(__uint_as_float(v[b + 2]) * sc, __uint_as_float(v[b + 3]) * sc);
+                    o.z = pack_bf16x2(__uint_as_float(v[b + 4]) * sc, __uint_as_float(v[b + 5]) * sc);
+                    o.w = pack_bf16x2(__uint_as_float(v[b + 6]) * sc, __uint_as_float(v[b + 7]) * sc);
+                    *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
+                }
+                __syncwarp();
+                const int j = lane & 7;
+                const int col = col0 + j * 8;
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int row = (lane >> 3) + 4 * it;
+                    const uint4 o = *reinterpret_cast<const uint4*>(stg + row * 128 + ((j ^ (row & 7)) << 4));
+                    if (drow[it] && col < ncols) {
+                        if (KIND == KIND_RAGGED_M && p.combine_out) red_add_bf16x8(drow[it] + col, o);
+                        else st_global_16_policy(drow[it] + col, o, out_pol);
+                    }
+                }
+                __syncwarp();
             };
             // (dense operands only: the 10-warp gather kernels have no registers to spare)
             if constexpr (KIND == KIND_RAGGED_M && !Tr::kAnyGather) if (p.swiglu_h) {
@@ -866,10 +920,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 tmem_ld_wait();
                 if (c == kBN / kColsPerWait - 1) release_acc();
                 const int col0 = ti.n0 + c * kColsPerWait;
-                store_chunk(v0, col0);
-                store_chunk(v1, col0 + 32);
-                store_chunk(v2, col0 + 64);
-                store_chunk(v3, col0 + 96);
+                if (staged) {
+                    store_act32(v0, col0);
+                    store_act32(v1, col0 + 32);
+                    store_out64_staged(v0, v1, col0);
+                    store_act32(v2, col0 + 64);
+                    store_act32(v3, col0 + 96);
+                    store_out64_staged(v2, v3, col0 + 64);
+                } else {
+                    store_act32(v0, col0);
+                    store_out32(v0, col0);
+                    store_act32(v1, col0 + 32);
+                    store_out32(v1, col0 + 32);
+                    store_act32(v2, col0 + 64);
+                    store_out32(v2, col0 + 64);
+                    store_act32(v3, col0 + 96);
+                    store_out32(v3, col0 + 96);
+                }
             }
             ++acc_count;
         }
