@@ -25,7 +25,8 @@
  *    (16-byte rows), every tensor pointer 16-byte aligned, E <= GG_MAX_EXPERTS,
  *    topk <= GG_MAX_TOPK, R < 2^31.
  *  - An empty problem (no rows or no output columns) returns GG_OK without a
- *    launch; an empty reduction writes zeros.
+ *    launch; an empty reduction writes zeros, and then the inputs that have
+ *    no elements (the reduced-over operands) may be NULL.
  *
  * Sources cited below (page title, then section):
  *  [U] unslothai--unsloth unsloth/kernels/moe/grouped_gemm/interface.py

@@ -32,7 +32,7 @@ def df32(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev())
 
 
-def assert_close(got_u16, ref, what, tight=True, magnitude=None):
+def assert_close(got_u16, ref, what, tight=True, magnitude=None, rel_fro=None):
     """Spec tolerance (max-abs <= 2e-2, rel-Frobenius <= 1e-2) and an
     elementwise bound of 2^-8 * magnitude + 1e-3 rms(ref): one bf16 rounding
     plus fp32 summation noise, small enough that any wrong, missing or
@@ -49,7 +49,10 @@ def assert_close(got_u16, ref, what, tight=True, magnitude=None):
     rf = float(np.linalg.norm(d)) / nrm if nrm > 0 else float(np.linalg.norm(d))
     assert np.isfinite(g).all(), "%s: non-finite output" % what
     assert ma <= MAX_ABS, "%s: max-abs error %.4g" % (what, ma)
-    assert rf <= REL_FRO, "%s: rel-Frobenius error %.4g" % (what, rf)
+    # rel_fro: the limit for an output whose arithmetic is not fp32 accumulation
+    # (the caller derives it from that arithmetic); default the spec limit
+    lim = REL_FRO if rel_fro is None else rel_fro
+    assert rf <= lim, "%s: rel-Frobenius error %.4g (limit %.4g)" % (what, rf, lim)
     if tight:
         rms = float(np.sqrt(np.mean(ref * ref)))
         bound = 2.0 ** -8 * np.abs(ref) + 1e-3 * rms + 1e-30

@@ -199,7 +199,85 @@ def test_gemms_max_experts():
     ref = orc.forward_combine(X2, W2, ro2["m_sizes"], ro2["gather_idx"], w2, T2, k2, 1)
     slots = orc.forward(X2, W2, ro2["m_sizes"], ro2["gather_idx"], w2, T2, k2, 1, 1, 1)
     mag = np.abs(slots).reshape(T2, k2, N).sum(axis=1)
-    assert_close(hbf(out), ref, "forward_combine topk=64", magnitude=(k2 + 1) / 4.0 * mag)
+    # 64 bf16 atomic adds per element: the fp32-accumulate rel-Frobenius limit does not
+    # apply; the limit is the Frobenius norm of the elementwise (topk+1) 2^-9 sum|w y|
+    fro_lim = float(np.linalg.norm((k2 + 1) * 2.0 ** -9 * mag) / np.linalg.norm(ref))
+    assert_close(hbf(out), ref, "forward_combine topk=64", magnitude=(k2 + 1) / 4.0 * mag,
+                 rel_fro=max(fro_lim, 1e-2))
+    assert status_of(st) == 0
+
+
+def _nan_filled(*shape):
+    """A bf16 buffer of NaNs: any element a call leaves untouched stays NaN."""
+    return torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda:0")
+
+
+def test_degenerate_shapes_write_what_they_document():
+    """Empty problems return without touching outputs; an empty reduction writes
+    zeros (forward with K = 0, dX with N = 0, dW with no routed rows); a
+    single-expert routing leaves every other expert's dW zero."""
+    E, topk = 4, 2
+    st = status_tensor()
+    # T = 0: route gives zero histogram and offsets; GEMMs are no-ops
+    r0 = gg.route_hist_offsets(torch.zeros(0, topk, dtype=torch.int32, device="cuda:0"), E, status=st)
+    assert r0["m_sizes"].cpu().tolist() == [0] * E and r0["offsets"].cpu().tolist() == [0] * (E + 1)
+    W = dbf(synth.normal_bf16(61, "dw", (E, 16, 8), 0.1))
+    Y0 = gg.forward(torch.zeros(0, 8, dtype=torch.bfloat16, device="cuda:0"), W, r0["m_sizes"],
+                    r0["gather_idx"], None, topk, status=st)
+    assert Y0.shape == (0, 16)
+    # K = 0 forward: zeros (and the fused combine and the SwiGLU activation likewise)
+    T = 5
+    ids = _ids(T, topk, E, 62)
+    r = _route_gpu(ids, E)
+    Wk0 = torch.zeros(E, 16, 0, dtype=torch.bfloat16, device="cuda:0")
+    Xk0 = torch.zeros(T * topk, 0, dtype=torch.bfloat16, device="cuda:0")
+    Y = _nan_filled(T * topk, 16)
+    gg.forward(Xk0, Wk0, r["m_sizes"], r["gather_idx"], None, topk, out=Y, status=st)
+    assert (Y.float() == 0).all()
+    Hy, A = _nan_filled(T * topk, 16), _nan_filled(T * topk, 8)
+    gg.forward_swiglu(Xk0, Wk0, r["m_sizes"], r["gather_idx"], topk, out=Hy, out_act=A, status=st)
+    assert (Hy.float() == 0).all() and (A.float() == 0).all()
+    out = _nan_filled(T, 16)
+    gg.forward_combine(Xk0, Wk0, r["m_sizes"], r["gather_idx"], None, topk, out=out, status=st)
+    assert (out.float() == 0).all()
+    # N = 0 dX: zeros; and the fused SwiGLU backward gives dH = 0
+    Wn0 = torch.zeros(E, 0, 8, dtype=torch.bfloat16, device="cuda:0")
+    dYn0 = torch.zeros(T * topk, 0, dtype=torch.bfloat16, device="cuda:0")
+    dX = _nan_filled(T * topk, 8)
+    gg.backward_dX(dYn0, Wn0, r["m_sizes"], r["gather_idx"], T, topk, out=dX, status=st)
+    assert (dX.float() == 0).all()
+    H = dbf(synth.normal_bf16(63, "dh", (T * topk, 16), 1.0))
+    dH = _nan_filled(T * topk, 16)
+    gg.backward_dX_swiglu(dYn0, Wn0, r["m_sizes"], topk, H, out=dH, status=st)
+    assert (dH.float() == 0).all()
+    # dW with no routed rows: zeros
+    dW = _nan_filled(E, 16, 8)
+    gg.backward_dW(torch.zeros(0, 8, dtype=torch.bfloat16, device="cuda:0"),
+                   torch.zeros(0, 16, dtype=torch.bfloat16, device="cuda:0"), r0["m_sizes"],
+                   r0["gather_idx"], 0, topk, out=dW, status=st)
+    assert (dW.float() == 0).all()
+    # dual GEMM with k = 0: both products zero
+    Yd0, Yd1 = _nan_filled(16, 24), _nan_filled(8, 32)
+    z = lambda *sh: torch.zeros(*sh, dtype=torch.bfloat16, device="cuda:0")
+    gg.dual_asym(z(16, 0), z(8, 0), z(0, 24), z(0, 32), out0=Yd0, out1=Yd1, status=st)
+    assert (Yd0.float() == 0).all() and (Yd1.float() == 0).all()
+    assert status_of(st) == 0
+    # every slot on one expert: forward / dW exact against the oracle, other experts' dW zero
+    T1, K1, N1 = 150, 64, 256
+    ids1 = np.full((T1, topk), 3, np.int32)
+    ro1 = orc.route(ids1, T1, topk, E)
+    r1 = _route_gpu(ids1, E)
+    X1 = synth.normal_bf16(64, "ox", (T1 * topk, K1), 0.1)
+    W1 = synth.normal_bf16(65, "ow", (E, N1, K1), 0.1)
+    dY1 = synth.normal_bf16(66, "ody", (T1 * topk, N1), 0.1)
+    Y1 = gg.forward(dbf(X1), dbf(W1), r1["m_sizes"], r1["gather_idx"], None, topk, status=st)
+    assert_close(hbf(Y1), orc.forward(X1, W1, ro1["m_sizes"], ro1["gather_idx"], None, T1, topk, 0, 0, 0),
+                 "forward one expert")
+    dW1 = gg.backward_dW(dbf(X1), dbf(dY1), r1["m_sizes"], r1["gather_idx"], T1, topk, status=st)
+    ref = orc.backward_dW(X1, dY1, ro1["m_sizes"], ro1["gather_idx"], T1, topk, 0, 0)
+    assert_close(hbf(dW1), ref, "dW one expert")
+    got = hbf(dW1)
+    assert (got[[0, 1, 2]] == 0).all()
     assert status_of(st) == 0
 
 

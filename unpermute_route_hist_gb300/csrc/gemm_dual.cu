@@ -21,8 +21,12 @@ extern "C" int gg_dual_asym(const gg_bf16* X0, const gg_bf16* X1, const gg_bf16*
     if (m0 >= lim || m1 >= lim || k >= lim || n0 >= lim || n1 >= lim) return GG_ERR_UNSUPPORTED;
     const bool e0 = m0 == 0 || n0 == 0, e1 = m1 == 0 || n1 == 0;
     if (e0 && e1) return GG_OK;
-    if ((!e0 && (!X0 || !W0 || !Y0)) || (!e1 && (!X1 || !W1 || !Y1))) return GG_ERR_INVALID_ARG;
-    if ((!e0 && (!al16(X0) || !al16(W0) || !al16(Y0))) || (!e1 && (!al16(X1) || !al16(W1) || !al16(Y1))))
+    // with k == 0 the X and W operands have no elements (may be NULL)
+    const bool kz = k == 0;
+    if ((!e0 && (!Y0 || (!kz && (!X0 || !W0)))) || (!e1 && (!Y1 || (!kz && (!X1 || !W1)))))
+        return GG_ERR_INVALID_ARG;
+    if ((!e0 && (!al16(Y0) || (!kz && (!al16(X0) || !al16(W0))))) ||
+        (!e1 && (!al16(Y1) || (!kz && (!al16(X1) || !al16(W1))))))
         return GG_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (k == 0) {

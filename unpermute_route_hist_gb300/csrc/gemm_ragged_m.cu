@@ -51,14 +51,16 @@ int gg_forward(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
     if ((permute_x || permute_y) && !gather_idx) return GG_ERR_INVALID_ARG;
     if (fuse_mul_post && (!permute_y || !topk_w)) return GG_ERR_INVALID_ARG;
     if (R == 0 || N == 0) return GG_OK;
-    if (!X || !W || !m_sizes || !Y) return GG_ERR_INVALID_ARG;
-    if (!al16(X) || !al16(W) || !al16(Y)) return GG_ERR_UNSUPPORTED;
+    if (!m_sizes || !Y) return GG_ERR_INVALID_ARG;
+    if (!al16(Y)) return GG_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (K == 0) {
+    if (K == 0) {  // X and W have no elements (may be NULL)
         const cudaError_t e = cudaMemsetAsync(Y, 0, static_cast<size_t>(R * N) * 2, st);
         if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
         return GG_OK;
     }
+    if (!X || !W) return GG_ERR_INVALID_ARG;
+    if (!al16(X) || !al16(W)) return GG_ERR_UNSUPPORTED;
     GemmParams p = base_params(E, topk, R, m_sizes, gather_idx, status);
     p.N = static_cast<int>(N);
     p.Kred = static_cast<int>(K);
@@ -89,8 +91,10 @@ int gg_forward_swiglu(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes
         return GG_ERR_UNSUPPORTED;
     if (permute_x && !gather_idx) return GG_ERR_INVALID_ARG;
     if (R == 0 || N == 0) return GG_OK;
-    if (!X || !W || !m_sizes || !A) return GG_ERR_INVALID_ARG;
-    if (!al16(X) || !al16(W) || !al16(A) || (Y && !al16(Y))) return GG_ERR_UNSUPPORTED;
+    if (!m_sizes || !A) return GG_ERR_INVALID_ARG;
+    if (!al16(A) || (Y && !al16(Y))) return GG_ERR_UNSUPPORTED;
+    if (K > 0 && (!X || !W)) return GG_ERR_INVALID_ARG;  // with K == 0 they have no elements
+    if (K > 0 && (!al16(X) || !al16(W))) return GG_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) {  // y = 0, so silu(0) * 0 = 0
         cudaError_t e = cudaMemsetAsync(A, 0, static_cast<size_t>(R * (N / 2)) * 2, st);
@@ -127,8 +131,10 @@ int gg_forward_combine(const gg_bf16* X, const gg_bf16* W, const int32_t* m_size
     if (R >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
         return GG_ERR_UNSUPPORTED;
     if (T == 0 || N == 0) return GG_OK;
-    if (!X || !W || !m_sizes || !gather_idx || !out) return GG_ERR_INVALID_ARG;
-    if (!al16(X) || !al16(W) || !al16(out)) return GG_ERR_UNSUPPORTED;
+    if (!m_sizes || !gather_idx || !out) return GG_ERR_INVALID_ARG;
+    if (!al16(out)) return GG_ERR_UNSUPPORTED;
+    if (K > 0 && (!X || !W)) return GG_ERR_INVALID_ARG;  // with K == 0 they have no elements
+    if (K > 0 && (!al16(X) || !al16(W))) return GG_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the adds accumulate into a zeroed output (every token row gets topk adds)
     cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(T * N) * 2, st);
@@ -165,8 +171,10 @@ int gg_backward_dX(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes,
     if ((permute_x || permute_y) && !gather_idx) return GG_ERR_INVALID_ARG;
     if (dX_tok && !permute_x) return GG_ERR_INVALID_ARG;
     if (R == 0 || K == 0) return GG_OK;
-    if (!dY || !W || !m_sizes || !dX) return GG_ERR_INVALID_ARG;
-    if (!al16(dY) || !al16(W) || !al16(dX) || (dX_tok && !al16(dX_tok))) return GG_ERR_UNSUPPORTED;
+    if (!m_sizes || !dX) return GG_ERR_INVALID_ARG;
+    if (!al16(dX) || (dX_tok && !al16(dX_tok))) return GG_ERR_UNSUPPORTED;
+    if (N > 0 && (!dY || !W)) return GG_ERR_INVALID_ARG;  // with N == 0 they have no elements
+    if (N > 0 && (!al16(dY) || !al16(W))) return GG_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int rc = GG_OK;
     if (N == 0) {
@@ -209,8 +217,10 @@ int gg_backward_dX_swiglu(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_
     if (R >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || 2 * K >= (int64_t(1) << 31))
         return GG_ERR_UNSUPPORTED;
     if (R == 0 || K == 0) return GG_OK;
-    if (!dY || !W || !m_sizes || !H || !dH) return GG_ERR_INVALID_ARG;
-    if (!al16(dY) || !al16(W) || !al16(H) || !al16(dH)) return GG_ERR_UNSUPPORTED;
+    if (!m_sizes || !dH) return GG_ERR_INVALID_ARG;
+    if (!al16(dH)) return GG_ERR_UNSUPPORTED;
+    if (N > 0 && (!dY || !W || !H)) return GG_ERR_INVALID_ARG;  // N == 0: dH = 0, no inputs read
+    if (N > 0 && (!al16(dY) || !al16(W) || !al16(H))) return GG_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (N == 0) {  // dA = 0, so dH = 0
         const cudaError_t e = cudaMemsetAsync(dH, 0, static_cast<size_t>(R * 2 * K) * 2, st);
