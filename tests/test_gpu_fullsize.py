@@ -2,7 +2,9 @@
 benchmark times: the whole MoE layer step (route, permute, forward, combine,
 backward dX with the token sum, backward dW) runs once on the GPU, then
 sampled outputs are computed one by one by the oracle from the same seeded
-host inputs.  Samples include every expert's first and last row and rows on
+host inputs.  The variants with the gather fused into the operand load (the
+forward's token gather, dX's slot gather, dW's token and slot gathers) are
+checked on the same samples.  Samples include every expert's first and last row and rows on
 both sides of each 128-row tile boundary, plus seeded random rows; for dW,
 rows of every non-empty expert, its first and last, and the largest expert.
 Integer outputs (routing, permute) are compared in full, bit for bit."""
@@ -70,6 +72,8 @@ def _run_layer(cfg):
                               status=st)
     res["dX1"], res["dXt"] = hbf(dX1), hbf(dXt)
     res["dW1"] = hbf(gg.backward_dW(Xp, dH, r["m_sizes"], r["gather_idx"], T, k, status=st))
+    res["dW1_fused"] = hbf(gg.backward_dW(X, dH, r["m_sizes"], r["gather_idx"], T, k, True, False,
+                                          status=st))
     if I:
         A2, W2, G = dbf(host["A2"]), dbf(host["W2"]), dbf(host["G"])
         wt = df32(w)
@@ -85,6 +89,8 @@ def _run_layer(cfg):
         res["dA2_fused"] = hbf(gg.backward_dX(dY2, W2, r["m_sizes"], r["gather_idx"], T, k, False, True,
                                               status=st))
         res["dW2"] = hbf(gg.backward_dW(A2, dYp, r["m_sizes"], r["gather_idx"], T, k, status=st))
+        res["dW2_fused"] = hbf(gg.backward_dW(A2, dY2, r["m_sizes"], r["gather_idx"], T, k, False, True,
+                                              status=st))
     for key in ("m_sizes", "offsets", "padded_offsets", "gather_idx", "row_id_map"):
         res[key] = r[key].cpu().numpy()
     res["status"] = status_of(st)
@@ -126,8 +132,9 @@ def test_full_layer_sampled(name):
     es, ns, empty = _sample_dw(m, N1, rng)
     vals = orc.backward_dW_rows(host["X"], host["dH"], m, g, k, 1, 0, es, ns)
     assert_close(res["dW1"][es, ns], vals, name + " dW1")
+    assert_close(res["dW1_fused"][es, ns], vals, name + " dW1 (fused token gather)")
     for e in empty:
-        assert (res["dW1"][e] == 0).all()
+        assert (res["dW1"][e] == 0).all() and (res["dW1_fused"][e] == 0).all()
 
     if I:
         # GEMM2 forward with the scatter to token order (and with the top-k scale)
@@ -164,8 +171,9 @@ def test_full_layer_sampled(name):
         es, ns, empty = _sample_dw(m, K, rng)
         vals = orc.backward_dW_rows(host["A2"], dY2h, m, g, k, 0, 1, es, ns)
         assert_close(res["dW2"][es, ns], vals, name + " dW2")
+        assert_close(res["dW2_fused"][es, ns], vals, name + " dW2 (fused slot gather)")
         for e in empty:
-            assert (res["dW2"][e] == 0).all()
+            assert (res["dW2"][e] == 0).all() and (res["dW2_fused"][e] == 0).all()
 
 
 def test_mlp8_gemm1_swiglu_sampled():
