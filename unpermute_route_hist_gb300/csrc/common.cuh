@@ -212,6 +212,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t cta)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(cta));
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
+// Arrive on the barrier at the same offset in CTA `cta` with the default
+// (release, CTA-scope) semantics: for a hand-off whose data needs no
+// cluster-wide memory ordering (TMEM reads that completed before the arrive),
+// it avoids the cost of a cluster-scope release behind the thread's
+// outstanding global stores.
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t* bar, uint32_t cta) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(cta));
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
 // Shared::cluster address of the variable at the same offset in CTA `cta`.
 __device__ __forceinline__ uint32_t mapa_u32(const void* p, uint32_t cta) {
     uint32_t remote;

@@ -744,12 +744,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             const uint32_t acc_phase = (acc_count >> 1) & 1u;
             if (!warp_wait(&ctl->tmem_full[buf], acc_phase, abort_flag, p.status, 64, PAIR)) break;
             tc_fence_after();
-            // hand the accumulator back to the MMA issuer (the even CTA's, for a pair)
+            // hand the accumulator back to the MMA issuer (the even CTA's, for a pair).
+            // The TMEM loads have completed (tcgen05.wait::ld) before the arrive, so
+            // it needs no cluster-scope release: that would wait for this thread's
+            // global stores in flight.
             auto release_acc = [&]() {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    if (PAIR) mbar_arrive_cluster(&ctl->tmem_empty[buf], 0);
+                    if (PAIR && rank != 0) mbar_arrive_remote(&ctl->tmem_empty[buf], 0);
                     else mbar_arrive(&ctl->tmem_empty[buf]);
                 }
             };
@@ -834,13 +837,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 __syncwarp();
                 const int j = lane & 7;
                 const int col = col0 + j * 8;
+                // all eight shared-memory reads are issued before the first global
+                // store (the stores' memory clobber would otherwise serialise each
+                // read's latency behind the previous store)
+                uint4 o[8];
 #pragma unroll
                 for (int it = 0; it < 8; ++it) {
                     const int row = (lane >> 3) + 4 * it;
-                    const uint4 o = *reinterpret_cast<const uint4*>(stg + row * 128 + ((j ^ (row & 7)) << 4));
+                    o[it] = *reinterpret_cast<const uint4*>(stg + row * 128 + ((j ^ (row & 7)) << 4));
+                }
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
                     if (drow[it] && col < ncols) {
-                        if (KIND == KIND_RAGGED_M && p.combine_out) red_add_bf16x8(drow[it] + col, o);
-                        else st_global_16_policy(drow[it] + col, o, out_pol);
+                        if (KIND == KIND_RAGGED_M && p.combine_out) red_add_bf16x8(drow[it] + col, o[it]);
+                        else st_global_16_policy(drow[it] + col, o[it], out_pol);
                     }
                 }
                 __syncwarp();
