@@ -18,12 +18,13 @@
 // stages fit), the even CTA issues the MMA for both, and each CTA's tensor
 // memory holds the accumulator of its own 128 rows.  Warp roles:
 //   warp 0      tile scheduler + TMA producer (lane 0) for dense operands
-//   warp 1      TMEM allocation + MMA issue (lane 0); zeroes ragged tails
-//               (PAIR, odd CTA: zeroes its own ragged tails and forwards the
-//               stage's readiness to the even CTA)
+//   warp 1      TMEM allocation + MMA issue (lane 0 alone; single-CTA dW: the
+//               whole warp joins at a ragged tail stage to zero it)
 //   warps 2-5   epilogue: TMEM -> registers -> scale -> bf16 -> global rows
 //   warps 6-9   (only with a gathered operand) cp.async row-gather producers;
 //               each thread's copies arrive on the stage barrier as they land
+//   warp 6      (PAIR dW) ragged tail stages: zeroes this CTA's rows past the
+//               expert's end and signals the even CTA's issuer
 // Every role walks the same static tile list (slot + j*nslot, per CTA or cluster),
 // decoded from m_sizes in shared memory, so no role sends tile ids to another.
 //
@@ -117,7 +118,8 @@ struct TileInfo {
 struct SharedCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    uint64_t pfull[kMaxStages];  // PAIR dW, even CTA: the odd CTA's tail stage is ready
+    uint64_t pfull[kMaxStages];  // PAIR dW, even CTA: both CTAs' halves of a tail stage are zeroed
+    uint64_t tfull[kMaxStages];  // PAIR dW: this CTA's copies of a tail stage have landed
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t drain;
@@ -238,7 +240,7 @@ struct GemmTraits {
     static_assert(!(PAIR && KIND == KIND_DUAL), "the dual GEMM runs on single CTAs");
     static constexpr bool kAnyGather = A_GATHER || B_GATHER;
     static constexpr bool kCpGatherFence = kAnyGather;  // cp.async-written stages
-    static constexpr int kThreads = 32 * (6 + (kAnyGather ? kGatherWarps : 0));
+    static constexpr int kThreads = 32 * (6 + (kAnyGather ? kGatherWarps : 0) + (PAIR && KIND == KIND_RAGGED_K ? 1 : 0));
     static constexpr int kStages = PAIR ? 6 : 4;
     static constexpr int kBRows = PAIR ? kBN / 2 : kBN;  // B tile rows (n) held by one CTA
     static constexpr uint32_t kBBytes = kBRows * kBK * 2;
@@ -247,9 +249,10 @@ struct GemmTraits {
     static constexpr uint32_t kTmaBytes = (A_GATHER ? 0u : kABytes) + (B_GATHER ? 0u : kBBytes);
     static constexpr uint32_t kFullCount = 1 + (kAnyGather ? kGatherWarps * 32 : 0);
     // PAIR: both CTAs' TMA bytes of a stage complete on the even CTA's barrier,
-    // except for a ragged reduction's tail stage (dW): there each CTA zeroes its
-    // own tail rows before the MMA, so the odd CTA's copies complete on its own
-    // barrier and the odd CTA then signals the even one (pfull).
+    // except for a ragged reduction's tail stage (dW): there each CTA's copies
+    // complete on its own tail barrier (tfull), an extra warp of each CTA zeroes
+    // the rows past the expert's end, and both signal the even CTA (pfull).  The
+    // MMA issuer stays a single thread that only waits.
     static constexpr bool kTailFwd = PAIR && KIND == KIND_RAGGED_K;
     // pair kernels with ragged rows stage each epilogue warp's rows in shared memory
     // (4 KB a warp) so that global stores go out as whole 128-byte row segments (dW's
@@ -323,7 +326,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl->full[s], Tr::kFullCount);
             mbar_init(&ctl->empty[s], 1);
-            mbar_init(&ctl->pfull[s], 1);
+            mbar_init(&ctl->pfull[s], 2);  // the two CTAs' tail helpers
+            mbar_init(&ctl->tfull[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tmem_full[b], 1);
@@ -419,6 +423,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     const int64_t total_tiles = ctl->total_tiles;
     const uint32_t stage0 = smem_u32(stage_base);
 
+    // Rows [valid, zr_end) of a stage's dense operands hold the next expert's
+    // reduction rows: overwrite them with zeros (both operands, so no 0 * inf).
+    auto zero_tail = [&](int stage, int valid, int zr_end) {
+        const int nz = zr_end - valid;
+        if (nz <= 0) return;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        uint8_t* st = stage_base + stage * kStageBytes;
+        if (!A_GATHER) {
+            for (int idx = lane; idx < nz * (kBM / 64) * 8; idx += 32) {
+                const int piece = idx & 7, rest = idx >> 3;
+                const int cc = rest % (kBM / 64), r = valid + rest / (kBM / 64);
+                *reinterpret_cast<uint4*>(st + cc * kBK * 128 + r * 128 + piece * 16) = z;
+            }
+        }
+        if (!B_GATHER) {
+            for (int idx = lane; idx < nz * (Tr::kBRows / 64) * 8; idx += 32) {
+                const int piece = idx & 7, rest = idx >> 3;
+                const int cc = rest % (Tr::kBRows / 64), r = valid + rest / (Tr::kBRows / 64);
+                *reinterpret_cast<uint4*>(st + kABytes + cc * kBK * 128 + r * 128 + piece * 16) = z;
+            }
+        }
+        fence_proxy_async_smem();
+    };
+
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
@@ -442,8 +470,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         const bool tail = Tr::kTailFwd && ti.red_len - kb * kBK < kBK;
                         uint32_t bar;
                         if (tail) {
-                            mbar_arrive_expect_tx(&ctl->full[stage], kStageBytes);
-                            bar = mapa_u32(&ctl->full[stage], rank);
+                            // this CTA's copies land on its own tail barrier (its helper
+                            // warp zeroes the rows past the expert's end); the even CTA's
+                            // full barrier completes this phase with the producer's arrival
+                            if (leader) mbar_arrive(&ctl->full[stage]);
+                            mbar_arrive_expect_tx(&ctl->tfull[stage], kStageBytes);
+                            bar = mapa_u32(&ctl->tfull[stage], rank);
                         } else {
                             if (leader) mbar_arrive_expect_tx(&ctl->full[stage], 2 * kStageBytes);
                             bar = mapa_u32(&ctl->full[stage], 0);
@@ -526,37 +558,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             }
         }
     } else if (warp == 1) {
-        // Rows [valid, zr_end) of a stage's dense operands hold the next expert's
-        // reduction rows: overwrite them with zeros (both operands, so no 0 * inf).
-        auto zero_tail = [&](int stage, int valid, int zr_end) {
-            const int nz = zr_end - valid;
-            if (nz <= 0) return;
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            uint8_t* st = stage_base + stage * kStageBytes;
-            if (!A_GATHER) {
-                for (int idx = lane; idx < nz * (kBM / 64) * 8; idx += 32) {
-                    const int piece = idx & 7, rest = idx >> 3;
-                    const int cc = rest % (kBM / 64), r = valid + rest / (kBM / 64);
-                    *reinterpret_cast<uint4*>(st + cc * kBK * 128 + r * 128 + piece * 16) = z;
-                }
-            }
-            if (!B_GATHER) {
-                for (int idx = lane; idx < nz * (Tr::kBRows / 64) * 8; idx += 32) {
-                    const int piece = idx & 7, rest = idx >> 3;
-                    const int cc = rest % (Tr::kBRows / 64), r = valid + rest / (Tr::kBRows / 64);
-                    *reinterpret_cast<uint4*>(st + kABytes + cc * kBK * 128 + r * 128 + piece * 16) = z;
-                }
-            }
-            fence_proxy_async_smem();
-        };
-        if ((!PAIR || leader) && KIND != KIND_RAGGED_K) {
+        if ((!PAIR || leader) && (KIND != KIND_RAGGED_K || Tr::kTailFwd)) {
             // ------------------------------------ MMA issuer (lane 0 alone) --
-            // No stage needs the warp (no ragged tails to zero), so lane 0 runs
-            // the loop by itself: no per-stage shuffle or warp barrier between
-            // one stage's MMAs and the next.
+            // No stage needs the warp (no ragged tails to zero here; a dW pair's
+            // tails are zeroed by warp 6 of each CTA), so lane 0 runs the loop by
+            // itself: no per-stage shuffle or warp barrier between one stage's
+            // MMAs and the next.
             if (lane == 0) {
                 int stage = 0;
                 uint32_t phase = 0;
+                uint32_t pfull_par = 0;  // per-slot parity of pfull (tail stages only)
                 uint32_t acc_count = 0;
                 bool ok = true, any_mma = false;
                 for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
@@ -570,7 +581,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * kBN;
-                    for (int kb = 0; kb < ti.nkb; ++kb) {
+                    // a dW pair's ragged tail stage (the last, partly filled reduction
+                    // block) is issued after the loop, so the per-stage path carries no
+                    // tail test: the issue latency after a stage lands is the critical path
+                    const int nfull = Tr::kTailFwd ? static_cast<int>(ti.red_len / kBK) : ti.nkb;
+                    for (int kb = 0; kb < nfull; ++kb) {
                         if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.status)) { ok = false; break; }
                         tc_fence_after();
                         // cp.async writes are generic-proxy; order them before the
@@ -591,6 +606,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         if (++stage == kStages) { stage = 0; phase ^= 1u; }
                     }
                     if (!ok) break;
+                    if constexpr (Tr::kTailFwd) if (nfull < ti.nkb) {
+                        // both CTAs' halves of the tail stage have landed and were zeroed
+                        const int valid = static_cast<int>(ti.red_len - static_cast<int64_t>(nfull) * kBK);
+                        if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.status) ||
+                            !mbar_wait(&ctl->pfull[stage], (pfull_par >> stage) & 1u, abort_flag, p.status, 0,
+                                       kWaitLimitNs, true)) {
+                            ok = false;
+                            break;
+                        }
+                        pfull_par ^= 1u << stage;
+                        tc_fence_after();
+                        const uint32_t sA = stage0 + stage * kStageBytes;
+                        const uint32_t sB = sA + kABytes;
+                        for (int ks = 0; ks < (valid + 15) / 16; ++ks) {
+                            const uint64_t ad = operand_desc<A_MN>(sA, ks), bd = operand_desc<B_MN>(sB, ks);
+                            umma_bf16_pair(d_tmem, ad, bd, Tr::kIdesc, (nfull > 0 || ks > 0) ? 1u : 0u);
+                        }
+                        umma_commit_pair(&ctl->empty[stage], 0x3);
+                        any_mma = true;
+                        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    }
                     if (PAIR) umma_commit_pair(&ctl->tmem_full[buf], 0x3);
                     else umma_commit(&ctl->tmem_full[buf]);
                     ++acc_count;
@@ -604,15 +640,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 }
             }
             __syncwarp();
-        } else if (!PAIR || leader) {
-            // ------------------------- MMA issuer with ragged tails (dW) --
+        } else if (!PAIR) {
+            // ------------- MMA issuer with ragged tails (single-CTA dW) --
             // Lane 0 waits and issues; the other lanes join it only at a tail
             // stage, to zero the rows past the expert's end.  Every lane walks the
             // same loop (no early exit), so the warp-wide steps at tail stages
             // always match up, also after lane 0 has given up on a wait.
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t pfull_par = 0;  // per-slot parity of pfull (tail stages only)
             uint32_t acc_count = 0;
             bool ok = true, any_mma = false;
             for (int64_t t = slot; t < total_tiles; t += nslot) {
@@ -636,11 +671,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         // lane 0 has seen the stage land (or given up)
                         if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) zero_tail(stage, valid, ksteps * 16);
                         __syncwarp();
-                        if (Tr::kTailFwd && lane == 0) {
-                            // the odd CTA's half of this stage has landed, tail zeroed
-                            if (ok) ok = mbar_wait(&ctl->pfull[stage], (pfull_par >> stage) & 1u, abort_flag, p.status, 0, kWaitLimitNs, true);
-                            pfull_par ^= 1u << stage;
-                        }
                     }
                     if (lane == 0 && ok) {
                         tc_fence_after();
@@ -649,50 +679,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         if (Tr::kAnyGather) fence_proxy_async_smem();
                         for (int ks = 0; ks < ksteps; ++ks) {
                             const uint64_t ad = operand_desc<A_MN>(sA, ks), bd = operand_desc<B_MN>(sB, ks);
-                            const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-                            if (PAIR) umma_bf16_pair(d_tmem, ad, bd, Tr::kIdesc, acc);
-                            else umma_bf16(d_tmem, ad, bd, Tr::kIdesc, acc);
+                            umma_bf16(d_tmem, ad, bd, Tr::kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
                         }
-                        if (PAIR) umma_commit_pair(&ctl->empty[stage], 0x3);
-                        else umma_commit(&ctl->empty[stage]);
+                        umma_commit(&ctl->empty[stage]);
                         any_mma = true;
                     }
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
-                if (lane == 0 && ok) {
-                    if (PAIR) umma_commit_pair(&ctl->tmem_full[buf], 0x3);
-                    else umma_commit(&ctl->tmem_full[buf]);
-                }
+                if (lane == 0 && ok) umma_commit(&ctl->tmem_full[buf]);
                 ++acc_count;
             }
             // All MMAs of this thread finish before TMEM is released.
             if (lane == 0 && any_mma) {
-                if (PAIR) umma_commit_pair(&ctl->drain, 0x1);
-                else umma_commit(&ctl->drain);
+                umma_commit(&ctl->drain);
                 int dummy = 0;
                 mbar_wait(&ctl->drain, 0, reinterpret_cast<volatile int*>(&dummy), p.status);
             }
             __syncwarp();
-        } else if (Tr::kTailFwd) {
-            // --------------------- odd CTA of a dW pair: tail stages only --
-            int stage = 0;
-            uint32_t full_par = 0;  // per-slot parity of this CTA's own full barriers
-            bool ok = true;
-            for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
-                const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
-                for (int kb = 0; kb < ti.nkb; ++kb) {
-                    const int valid = min(kBK, ti.red_len - kb * kBK);
-                    if (valid < kBK) {
-                        if (!warp_wait(&ctl->full[stage], (full_par >> stage) & 1u, abort_flag, p.status)) { ok = false; break; }
-                        full_par ^= 1u << stage;
-                        zero_tail(stage, valid, ((valid + 15) / 16) * 16);
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(&ctl->pfull[stage], 0);
-                        __syncwarp();
-                    }
-                    if (++stage == kStages) stage = 0;
-                }
-            }
         }
     } else if (warp < 6) {
         // ----------------------------------------------------- epilogue --
@@ -949,6 +952,35 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 }
             }
             ++acc_count;
+        }
+    } else if (Tr::kTailFwd) {
+        // ---------------------------- warp 6 of a dW pair: ragged tail stages --
+        // Walks the producer's stage sequence; at each tail stage it waits for
+        // this CTA's copies (tfull: used by tail stages only, so its per-slot
+        // parity flips once per tail use), zeroes the rows past the expert's end
+        // in this CTA's operands, and signals the even CTA's issuer (pfull counts
+        // both CTAs).  The odd CTA's signal is a cluster-scope release: its zeroed
+        // rows are read by the pair's MMA issued from the even CTA.
+        int stage = 0;
+        uint32_t tpar = 0;
+        bool ok = true;
+        for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
+            const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
+            for (int kb = 0; kb < ti.nkb; ++kb) {
+                const int valid = min(kBK, ti.red_len - kb * kBK);
+                if (valid < kBK) {
+                    if (!warp_wait(&ctl->tfull[stage], (tpar >> stage) & 1u, abort_flag, p.status)) { ok = false; break; }
+                    tpar ^= 1u << stage;
+                    zero_tail(stage, valid, ((valid + 15) / 16) * 16);
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (leader) mbar_arrive(&ctl->pfull[stage]);
+                        else mbar_arrive_cluster(&ctl->pfull[stage], 0);
+                    }
+                    __syncwarp();
+                }
+                if (++stage == kStages) stage = 0;
+            }
         }
     } else {
         // ---------------------------------------------- gather producers --
