@@ -118,8 +118,9 @@ struct TileInfo {
 struct SharedCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    uint64_t pfull[kMaxStages];  // PAIR dW, even CTA: both CTAs' halves of a tail stage are zeroed
-    uint64_t tfull[kMaxStages];  // PAIR dW: this CTA's copies of a tail stage have landed
+    uint64_t tfull;   // PAIR dW: this CTA's copies of a tile's tail block have landed
+    uint64_t pfull;   // PAIR dW, even CTA: both CTAs' tail halves are zeroed
+    uint64_t tempty;  // PAIR dW: the tail buffer's MMAs have completed
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t drain;
@@ -241,7 +242,11 @@ struct GemmTraits {
     static constexpr bool kAnyGather = A_GATHER || B_GATHER;
     static constexpr bool kCpGatherFence = kAnyGather;  // cp.async-written stages
     static constexpr int kThreads = 32 * (6 + (kAnyGather ? kGatherWarps : 0) + (PAIR && KIND == KIND_RAGGED_K ? 1 : 0));
-    static constexpr int kStages = PAIR ? 6 : 4;
+    // PAIR dW: a five-stage ring plus one buffer for each tile's ragged tail
+    // block, which is loaded a few stages into the tile and consumed last
+    // (its rows past the expert's end are zeroed meanwhile).
+    static constexpr int kStages = PAIR ? (KIND == KIND_RAGGED_K ? 5 : 6) : 4;
+    static constexpr int kBufStages = kStages + (PAIR && KIND == KIND_RAGGED_K ? 1 : 0);
     static constexpr int kBRows = PAIR ? kBN / 2 : kBN;  // B tile rows (n) held by one CTA
     static constexpr uint32_t kBBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
@@ -249,10 +254,11 @@ struct GemmTraits {
     static constexpr uint32_t kTmaBytes = (A_GATHER ? 0u : kABytes) + (B_GATHER ? 0u : kBBytes);
     static constexpr uint32_t kFullCount = 1 + (kAnyGather ? kGatherWarps * 32 : 0);
     // PAIR: both CTAs' TMA bytes of a stage complete on the even CTA's barrier,
-    // except for a ragged reduction's tail stage (dW): there each CTA's copies
-    // complete on its own tail barrier (tfull), an extra warp of each CTA zeroes
-    // the rows past the expert's end, and both signal the even CTA (pfull).  The
-    // MMA issuer stays a single thread that only waits.
+    // except for a ragged reduction's tail block (dW): it goes to the tail
+    // buffer, each CTA's copies complete on its own tail barrier (tfull), an
+    // extra warp of each CTA zeroes the rows past the expert's end, and both
+    // signal the even CTA (pfull).  The MMA issuer stays a single thread that
+    // only waits.
     static constexpr bool kTailFwd = PAIR && KIND == KIND_RAGGED_K;
     // pair kernels with ragged rows stage each epilogue warp's rows in shared memory
     // (4 KB a warp) so that global stores go out as whole 128-byte row segments (dW's
@@ -308,7 +314,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     uint8_t* stage_base = smem;
     constexpr int kStages = Tr::kStages;
     constexpr uint32_t kStageBytes = Tr::kStageBytes;
-    uint8_t* epi_stage = smem + kStages * kStageBytes;  // kEpiStageBytes when Tr::kEpiStage
+    uint8_t* epi_stage = smem + Tr::kBufStages * kStageBytes;  // kEpiStageBytes when Tr::kEpiStage
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(epi_stage + (Tr::kEpiStage ? kEpiStageBytes : 0));
     int32_t* s_off = reinterpret_cast<int32_t*>(ctl + 1);
     int32_t* s_tp = s_off + (p.E + 1);
@@ -326,8 +332,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl->full[s], Tr::kFullCount);
             mbar_init(&ctl->empty[s], 1);
-            mbar_init(&ctl->pfull[s], 2);  // the two CTAs' tail helpers
-            mbar_init(&ctl->tfull[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tmem_full[b], 1);
@@ -335,6 +339,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             mbar_init(&ctl->tmem_empty[b], PAIR ? 8 : 4);
         }
         mbar_init(&ctl->drain, 1);
+        mbar_init(&ctl->tfull, 1);
+        mbar_init(&ctl->pfull, 2);  // the two CTAs' tail helpers
+        mbar_init(&ctl->tempty, 1);
         ctl->abort_flag = 0;
         fence_barrier_init();
     }
@@ -453,59 +460,67 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
+            uint32_t tail_uses = 0;  // PAIR dW: tail blocks issued so far
             bool ok = true;
             for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
                 const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
                 const CUtensorMap* mA = (KIND == KIND_DUAL && ti.e == 1) ? &tmA1 : &tmA0;
                 const CUtensorMap* mB = (KIND == KIND_DUAL && ti.e == 1) ? &tmB1 : &tmB0;
-                for (int kb = 0; kb < ti.nkb; ++kb) {
+                // PAIR: one reduction block into (sA, sB), completing on barrier `bar`
+                // (a shared::cluster address).  A: this CTA's own m-tile (an odd CTA
+                // past the expert's last m-tile still loads its box: those rows are
+                // never stored).  B: this CTA's half of the n-tile's columns.
+                auto load_pair = [&](uint8_t* sA, uint8_t* sB, uint32_t bar, int32_t red) {
+                    const int32_t nb = ti.n0 + static_cast<int32_t>(rank) * (kBN / 2);
+                    const bool chunk_view = KIND != KIND_DUAL && p.mn_chunk_view;
+                    if (!A_MN) {
+                        tma_load_2d_pair(sA, mA, bar, red, static_cast<int32_t>(ti.row0));
+                    } else if (chunk_view) {
+                        tma_load_3d_pair(sA, mA, bar, 0, red, static_cast<int32_t>(ti.row0 / 64));
+                    } else {
+#pragma unroll
+                        for (int cc = 0; cc < kBM / 64; ++cc)
+                            tma_load_2d_pair(sA + cc * kBK * 128, mA, bar, static_cast<int32_t>(ti.row0) + cc * 64, red);
+                    }
+                    if (!B_MN) {
+                        if (KIND == KIND_RAGGED_M) tma_load_3d_pair(sB, mB, bar, red, nb, ti.e);
+                        else tma_load_2d_pair(sB, mB, bar, red, nb);
+                    } else if (chunk_view) {
+                        if (KIND == KIND_RAGGED_M) tma_load_4d_pair(sB, mB, bar, 0, red, nb / 64, ti.e);
+                        else tma_load_3d_pair(sB, mB, bar, 0, red, nb / 64);
+                    } else {
+#pragma unroll
+                        for (int cc = 0; cc < Tr::kBRows / 64; ++cc) {
+                            if (KIND == KIND_RAGGED_M)
+                                tma_load_3d_pair(sB + cc * kBK * 128, mB, bar, nb + cc * 64, red, ti.e);
+                            else
+                                tma_load_2d_pair(sB + cc * kBK * 128, mB, bar, nb + cc * 64, red);
+                        }
+                    }
+                };
+                // PAIR dW: whole reduction blocks go through the ring; the ragged tail
+                // block (if any) goes to the tail buffer once kStages + 1 blocks of the
+                // tile are issued (or after the last whole block), by when the previous
+                // tile's tail has normally been consumed.
+                const int nfull = Tr::kTailFwd ? ti.red_len / kBK : ti.nkb;
+                const int tail_at = (Tr::kTailFwd && nfull < ti.nkb) ? min(nfull, kStages + 1) : -1;
+                for (int kb = 0; kb <= nfull; ++kb) {
+                    if (Tr::kTailFwd && kb == tail_at) {
+                        if (!mbar_wait(&ctl->tempty, (tail_uses & 1u) ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                        uint8_t* tA = stage_base + kStages * kStageBytes;
+                        mbar_arrive_expect_tx(&ctl->tfull, kStageBytes);
+                        load_pair(tA, tA + kABytes, mapa_u32(&ctl->tfull, rank),
+                                  static_cast<int32_t>(ti.red0 + static_cast<int64_t>(nfull) * kBK));
+                        ++tail_uses;
+                    }
+                    if (kb == nfull) break;
                     if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     uint8_t* sA = stage_base + stage * kStageBytes;
                     uint8_t* sB = sA + kABytes;
                     const int32_t red = static_cast<int32_t>(ti.red0 + static_cast<int64_t>(kb) * kBK);
                     if (PAIR) {
-                        // A: this CTA's own m-tile (an odd CTA past the expert's last
-                        // m-tile still loads its box: those rows are never stored).
-                        // B: this CTA's half of the n-tile's columns.
-                        const bool tail = Tr::kTailFwd && ti.red_len - kb * kBK < kBK;
-                        uint32_t bar;
-                        if (tail) {
-                            // this CTA's copies land on its own tail barrier (its helper
-                            // warp zeroes the rows past the expert's end); the even CTA's
-                            // full barrier completes this phase with the producer's arrival
-                            if (leader) mbar_arrive(&ctl->full[stage]);
-                            mbar_arrive_expect_tx(&ctl->tfull[stage], kStageBytes);
-                            bar = mapa_u32(&ctl->tfull[stage], rank);
-                        } else {
-                            if (leader) mbar_arrive_expect_tx(&ctl->full[stage], 2 * kStageBytes);
-                            bar = mapa_u32(&ctl->full[stage], 0);
-                        }
-                        const int32_t nb = ti.n0 + static_cast<int32_t>(rank) * (kBN / 2);
-                        const bool chunk_view = KIND != KIND_DUAL && p.mn_chunk_view;
-                        if (!A_MN) {
-                            tma_load_2d_pair(sA, mA, bar, red, static_cast<int32_t>(ti.row0));
-                        } else if (chunk_view) {
-                            tma_load_3d_pair(sA, mA, bar, 0, red, static_cast<int32_t>(ti.row0 / 64));
-                        } else {
-#pragma unroll
-                            for (int cc = 0; cc < kBM / 64; ++cc)
-                                tma_load_2d_pair(sA + cc * kBK * 128, mA, bar, static_cast<int32_t>(ti.row0) + cc * 64, red);
-                        }
-                        if (!B_MN) {
-                            if (KIND == KIND_RAGGED_M) tma_load_3d_pair(sB, mB, bar, red, nb, ti.e);
-                            else tma_load_2d_pair(sB, mB, bar, red, nb);
-                        } else if (chunk_view) {
-                            if (KIND == KIND_RAGGED_M) tma_load_4d_pair(sB, mB, bar, 0, red, nb / 64, ti.e);
-                            else tma_load_3d_pair(sB, mB, bar, 0, red, nb / 64);
-                        } else {
-#pragma unroll
-                            for (int cc = 0; cc < Tr::kBRows / 64; ++cc) {
-                                if (KIND == KIND_RAGGED_M)
-                                    tma_load_3d_pair(sB + cc * kBK * 128, mB, bar, nb + cc * 64, red, ti.e);
-                                else
-                                    tma_load_2d_pair(sB + cc * kBK * 128, mB, bar, nb + cc * 64, red);
-                            }
-                        }
+                        if (leader) mbar_arrive_expect_tx(&ctl->full[stage], 2 * kStageBytes);
+                        load_pair(sA, sB, mapa_u32(&ctl->full[stage], 0), red);
                     } else {
                         if (Tr::kTmaBytes) mbar_arrive_expect_tx(&ctl->full[stage], Tr::kTmaBytes);
                         else mbar_arrive(&ctl->full[stage]);
@@ -544,7 +559,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             }
             // Let every TMA copy this thread issued land before the CTA can exit.
             // (PAIR, odd CTA: its copies complete on the even CTA's barriers, or
-            // on its own tail barriers that its warp 1 waits for; the even CTA's
+            // on its own tail barrier that its warp 6 waits for; the even CTA's
             // MMAs consume all of them before the teardown's cluster barrier.)
             if (!PAIR || leader) {
                 const int64_t pend = issued < kStages ? issued : kStages;
@@ -567,7 +582,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             if (lane == 0) {
                 int stage = 0;
                 uint32_t phase = 0;
-                uint32_t pfull_par = 0;  // per-slot parity of pfull (tail stages only)
+                uint32_t tail_uses = 0;  // PAIR dW: tail blocks consumed so far
                 uint32_t acc_count = 0;
                 bool ok = true, any_mma = false;
                 for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
@@ -581,9 +596,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * kBN;
-                    // a dW pair's ragged tail stage (the last, partly filled reduction
-                    // block) is issued after the loop, so the per-stage path carries no
-                    // tail test: the issue latency after a stage lands is the critical path
+                    // a dW pair's ragged tail block (the last, partly filled one) comes
+                    // from the tail buffer after the loop, so the per-stage path carries
+                    // no tail test: the issue latency after a stage lands is the
+                    // critical path
                     const int nfull = Tr::kTailFwd ? static_cast<int>(ti.red_len / kBK) : ti.nkb;
                     for (int kb = 0; kb < nfull; ++kb) {
                         if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.status)) { ok = false; break; }
@@ -607,25 +623,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     }
                     if (!ok) break;
                     if constexpr (Tr::kTailFwd) if (nfull < ti.nkb) {
-                        // both CTAs' halves of the tail stage have landed and were zeroed
+                        // both CTAs' halves of the tail block have landed and were zeroed
                         const int valid = static_cast<int>(ti.red_len - static_cast<int64_t>(nfull) * kBK);
-                        if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.status) ||
-                            !mbar_wait(&ctl->pfull[stage], (pfull_par >> stage) & 1u, abort_flag, p.status, 0,
-                                       kWaitLimitNs, true)) {
+                        if (!mbar_wait(&ctl->pfull, tail_uses & 1u, abort_flag, p.status, 0, kWaitLimitNs, true)) {
                             ok = false;
                             break;
                         }
-                        pfull_par ^= 1u << stage;
+                        ++tail_uses;
                         tc_fence_after();
-                        const uint32_t sA = stage0 + stage * kStageBytes;
+                        const uint32_t sA = stage0 + kStages * kStageBytes;
                         const uint32_t sB = sA + kABytes;
                         for (int ks = 0; ks < (valid + 15) / 16; ++ks) {
                             const uint64_t ad = operand_desc<A_MN>(sA, ks), bd = operand_desc<B_MN>(sB, ks);
                             umma_bf16_pair(d_tmem, ad, bd, Tr::kIdesc, (nfull > 0 || ks > 0) ? 1u : 0u);
                         }
-                        umma_commit_pair(&ctl->empty[stage], 0x3);
+                        umma_commit_pair(&ctl->tempty, 0x3);  // the tail buffer is free in both CTAs
                         any_mma = true;
-                        if (++stage == kStages) { stage = 0; phase ^= 1u; }
                     }
                     if (PAIR) umma_commit_pair(&ctl->tmem_full[buf], 0x3);
                     else umma_commit(&ctl->tmem_full[buf]);
@@ -954,33 +967,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             ++acc_count;
         }
     } else if (Tr::kTailFwd) {
-        // ---------------------------- warp 6 of a dW pair: ragged tail stages --
-        // Walks the producer's stage sequence; at each tail stage it waits for
-        // this CTA's copies (tfull: used by tail stages only, so its per-slot
-        // parity flips once per tail use), zeroes the rows past the expert's end
-        // in this CTA's operands, and signals the even CTA's issuer (pfull counts
-        // both CTAs).  The odd CTA's signal is a cluster-scope release: its zeroed
-        // rows are read by the pair's MMA issued from the even CTA.
-        int stage = 0;
-        uint32_t tpar = 0;
-        bool ok = true;
-        for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
+        // ----------------------------- warp 6 of a dW pair: ragged tail blocks --
+        // For each tile with a tail block: wait for this CTA's copies of it (tfull,
+        // one phase per tail block), zero the rows past the expert's end in this
+        // CTA's operands, and signal the even CTA's issuer (pfull counts both
+        // CTAs).  The odd CTA's signal is a cluster-scope release: its zeroed rows
+        // are read by the pair's MMA issued from the even CTA.  The block was
+        // loaded a few stages into the tile and is consumed at its end, so this
+        // work overlaps the tile's main loop.
+        uint32_t tail_uses = 0;
+        for (int64_t t = slot; t < total_tiles; t += nslot) {
             const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
-            for (int kb = 0; kb < ti.nkb; ++kb) {
-                const int valid = min(kBK, ti.red_len - kb * kBK);
-                if (valid < kBK) {
-                    if (!warp_wait(&ctl->tfull[stage], (tpar >> stage) & 1u, abort_flag, p.status)) { ok = false; break; }
-                    tpar ^= 1u << stage;
-                    zero_tail(stage, valid, ((valid + 15) / 16) * 16);
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (leader) mbar_arrive(&ctl->pfull[stage]);
-                        else mbar_arrive_cluster(&ctl->pfull[stage], 0);
-                    }
-                    __syncwarp();
-                }
-                if (++stage == kStages) stage = 0;
+            const int nfull = ti.red_len / kBK;
+            if (nfull == ti.nkb) continue;
+            if (!warp_wait(&ctl->tfull, tail_uses & 1u, abort_flag, p.status)) break;
+            ++tail_uses;
+            zero_tail(kStages, ti.red_len - nfull * kBK, ((ti.red_len - nfull * kBK + 15) / 16) * 16);
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(&ctl->pfull);
+                else mbar_arrive_cluster(&ctl->pfull, 0);
             }
+            __syncwarp();
         }
     } else {
         // ---------------------------------------------- gather producers --
