@@ -359,6 +359,30 @@ def test_backward_dW(shape, px, py):
         assert (hbf(dW)[e] == 0).all()
 
 
+# Expert sizes around the ragged-reduction boundaries of dW's 2-CTA kernel: a tile's
+# whole 64-row blocks go through the stage ring and its partly filled last block (the
+# tail) through a separate buffer, issued after min(whole blocks, 6) of them.  The
+# sizes give 0-10 whole blocks with and without a tail, single rows, an empty expert,
+# and (N = 1088 -> 9 row tiles) pairs with a phantom half; about four tiles per pair,
+# so each pair runs several tails in a row.
+DW_TAIL_SIZES = [1, 63, 64, 65, 127, 128, 129, 191, 383, 384, 385, 447, 448, 449, 0, 17, 511, 513, 577, 640,
+                 641, 700]
+
+
+def test_backward_dW_tail_positions():
+    m = np.array(DW_TAIL_SIZES, np.int32)
+    E, R, N, K = m.size, int(m.sum()), 1088, 576
+    X = synth.normal_bf16(7, "tailx", (R, K), 0.1)
+    dY = synth.normal_bf16(8, "taily", (R, N), 0.1)
+    st = status_tensor()
+    dW = gg.backward_dW(dbf(X), dbf(dY), torch.from_numpy(m).to("cuda:0"), None, R, 1, status=st)
+    assert status_of(st) == 0
+    ref = orc.backward_dW(X, dY, m, None, R, 1, 0, 0)
+    got = hbf(dW)
+    assert_close(got, ref, "dW tail positions")
+    assert (got[m == 0] == 0).all()
+
+
 @pytest.mark.parametrize("px,store_y", [(0, True), (1, True), (1, False)])
 @pytest.mark.parametrize("T,topk,E,K,N", [(200, 2, 5, 320, 528), (64, 2, 4, 128, 256), (301, 3, 7, 136, 272)])
 def test_forward_swiglu(T, topk, E, K, N, px, store_y):
