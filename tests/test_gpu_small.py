@@ -452,7 +452,11 @@ def test_swiglu_bwd(rows, I):
 
 
 @pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])
-@pytest.mark.parametrize("dims", [(136, 72, 200, 264, 512), (512, 256, 1024, 2048, 4096), (8, 0, 64, 8, 16)])
+# The launch takes single-CTA 128 x 256 tiles when they fit one wave of SMs and
+# 2-CTA pairs beyond: (1032, 520, 136, 4104, 776) has 173 tiles, odd m-tile counts
+# (a phantom pair half in both problems) and partial n-tiles.
+@pytest.mark.parametrize("dims", [(136, 72, 200, 264, 512), (512, 256, 1024, 2048, 4096), (8, 0, 64, 8, 16),
+                                  (1032, 520, 136, 4104, 776)])
 def test_dual_asym(ta, tb, dims):
     m0, m1, k, n0, n1 = dims
     cfg = synth.DualConfig(m0=m0, m1=m1, k=k, n0=n0, n1=n1, seed=7)

@@ -238,7 +238,6 @@ __device__ __forceinline__ int64_t gather_row(const GemmParams& p, const GatherS
 template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR>
 struct GemmTraits {
     static_assert(!(PAIR && (A_GATHER || B_GATHER)), "2-CTA tiles are loaded by TMA only");
-    static_assert(!(PAIR && KIND == KIND_DUAL), "the dual GEMM runs on single CTAs");
     static constexpr bool kAnyGather = A_GATHER || B_GATHER;
     static constexpr bool kCpGatherFence = kAnyGather;  // cp.async-written stages
     static constexpr int kThreads = 32 * (6 + (kAnyGather ? kGatherWarps : 0) + (PAIR && KIND == KIND_RAGGED_K ? 1 : 0));
