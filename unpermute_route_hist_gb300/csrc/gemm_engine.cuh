@@ -755,6 +755,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 }
                 continue;
             }
+            // staged stores (below): the destination row pointers of the 8 rows each
+            // lane stores, gathered from their owners before the wait, so the work
+            // after the accumulator lands is TMEM loads and stores only
+            const bool staged = Tr::kEpiStage && out != nullptr;
+            uint8_t* stg = epi_stage + q * 4096;
+            uint16_t* drow[8];
+            if (staged) {
+                const uint64_t mine = reinterpret_cast<uint64_t>(orow);
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int src = (lane >> 3) + 4 * it;
+                    const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(mine), src);
+                    const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(mine >> 32), src);
+                    drow[it] = reinterpret_cast<uint16_t*>((static_cast<uint64_t>(hi) << 32) | lo);
+                }
+            }
             const uint32_t buf = acc_count & 1u;
             const uint32_t acc_phase = (acc_count >> 1) & 1u;
             if (!warp_wait(&ctl->tmem_full[buf], acc_phase, abort_flag, p.status, 64, PAIR)) break;
@@ -824,19 +840,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             // row, so neither phase has bank conflicts), then eight lanes per row write
             // four whole 128-byte row segments per store instruction.  Every lane of
             // the warp takes part (shuffles and warp barriers).
-            const bool staged = Tr::kEpiStage && out != nullptr;
-            uint8_t* stg = epi_stage + q * 4096;
-            uint16_t* drow[8];
-            if (staged) {
-                const uint64_t mine = reinterpret_cast<uint64_t>(orow);
-#pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int src = (lane >> 3) + 4 * it;
-                    const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(mine), src);
-                    const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(mine >> 32), src);
-                    drow[it] = reinterpret_cast<uint16_t*>((static_cast<uint64_t>(hi) << 32) | lo);
-                }
-            }
             auto store_out64_staged = [&](const uint32_t (&va)[32], const uint32_t (&vb)[32], int col0) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
