@@ -23,8 +23,9 @@
 //   warps 2-5   epilogue: TMEM -> registers -> scale -> bf16 -> global rows
 //   warps 6-9   (only with a gathered operand) cp.async row-gather producers;
 //               each thread's copies arrive on the stage barrier as they land
-//   warp 6      (PAIR dW) ragged tail stages: zeroes this CTA's rows past the
-//               expert's end and signals the even CTA's issuer
+//   warp 6      (PAIR dW) each tile's ragged tail block, loaded into its own
+//               buffer: zeroes this CTA's rows past the expert's end and
+//               signals the even CTA's issuer
 // Every role walks the same static tile list (slot + j*nslot, per CTA or cluster),
 // decoded from m_sizes in shared memory, so no role sends tile ids to another.
 //
@@ -258,7 +259,7 @@ struct GemmTraits {
     // extra warp of each CTA zeroes the rows past the expert's end, and both
     // signal the even CTA (pfull).  The MMA issuer stays a single thread that
     // only waits.
-    static constexpr bool kTailFwd = PAIR && KIND == KIND_RAGGED_K;
+    static constexpr bool kTailBuf = PAIR && KIND == KIND_RAGGED_K;
     // pair kernels with ragged rows stage each epilogue warp's rows in shared memory
     // (4 KB a warp) so that global stores go out as whole 128-byte row segments (dW's
     // tiles, long reductions sharing shared-memory bandwidth, measured faster without)
@@ -501,10 +502,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 // block (if any) goes to the tail buffer once kStages + 1 blocks of the
                 // tile are issued (or after the last whole block), by when the previous
                 // tile's tail has normally been consumed.
-                const int nfull = Tr::kTailFwd ? ti.red_len / kBK : ti.nkb;
-                const int tail_at = (Tr::kTailFwd && nfull < ti.nkb) ? min(nfull, kStages + 1) : -1;
+                const int nfull = Tr::kTailBuf ? ti.red_len / kBK : ti.nkb;
+                const int tail_at = (Tr::kTailBuf && nfull < ti.nkb) ? min(nfull, kStages + 1) : -1;
                 for (int kb = 0; kb <= nfull; ++kb) {
-                    if (Tr::kTailFwd && kb == tail_at) {
+                    if (Tr::kTailBuf && kb == tail_at) {
                         if (!mbar_wait(&ctl->tempty, (tail_uses & 1u) ^ 1u, abort_flag, p.status)) { ok = false; break; }
                         uint8_t* tA = stage_base + kStages * kStageBytes;
                         mbar_arrive_expect_tx(&ctl->tfull, kStageBytes);
@@ -572,7 +573,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             }
         }
     } else if (warp == 1) {
-        if ((!PAIR || leader) && (KIND != KIND_RAGGED_K || Tr::kTailFwd)) {
+        if ((!PAIR || leader) && (KIND != KIND_RAGGED_K || Tr::kTailBuf)) {
             // ------------------------------------ MMA issuer (lane 0 alone) --
             // No stage needs the warp (no ragged tails to zero here; a dW pair's
             // tails are zeroed by warp 6 of each CTA), so lane 0 runs the loop by
@@ -599,7 +600,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     // from the tail buffer after the loop, so the per-stage path carries
                     // no tail test: the issue latency after a stage lands is the
                     // critical path
-                    const int nfull = Tr::kTailFwd ? static_cast<int>(ti.red_len / kBK) : ti.nkb;
+                    const int nfull = Tr::kTailBuf ? static_cast<int>(ti.red_len / kBK) : ti.nkb;
                     for (int kb = 0; kb < nfull; ++kb) {
                         if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.status)) { ok = false; break; }
                         tc_fence_after();
@@ -621,7 +622,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         if (++stage == kStages) { stage = 0; phase ^= 1u; }
                     }
                     if (!ok) break;
-                    if constexpr (Tr::kTailFwd) if (nfull < ti.nkb) {
+                    if constexpr (Tr::kTailBuf) if (nfull < ti.nkb) {
                         // both CTAs' halves of the tail block have landed and were zeroed
                         const int valid = static_cast<int>(ti.red_len - static_cast<int64_t>(nfull) * kBK);
                         if (!mbar_wait(&ctl->pfull, tail_uses & 1u, abort_flag, p.status, 0, kWaitLimitNs, true)) {
@@ -968,7 +969,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             }
             ++acc_count;
         }
-    } else if (Tr::kTailFwd) {
+    } else if (Tr::kTailBuf) {
         // ----------------------------- warp 6 of a dW pair: ragged tail blocks --
         // For each tile with a tail block: wait for this CTA's copies of it (tfull,
         // one phase per tail block), zero the rows past the expert's end in this
