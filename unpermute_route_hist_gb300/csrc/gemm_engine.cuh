@@ -772,6 +772,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     drow[it] = reinterpret_cast<uint16_t*>((static_cast<uint64_t>(hi) << 32) | lo);
                 }
             }
+            // SwiGLU backward (dX with the stored H): this row's H values for the first
+            // kHAhead 16-column steps are loaded before the accumulator lands; each
+            // step then loads the step kHAhead further on, so the L2 latency of H is
+            // hidden behind four steps of work
+            constexpr int kHAhead = 4;
+            static_assert((kBN / 16) % kHAhead == 0, "whole groups of steps");
+            const uint16_t* hrow = nullptr;
+            uint4 hq[kHAhead][4];
+            auto load_h = [&](int col0, uint4 (&h)[4]) {
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd)
+                    if (col0 + qd * 4 < ncols) h[qd] = __ldg(reinterpret_cast<const uint4*>(hrow + 2 * col0 + qd * 8));
+            };
+            if constexpr (KIND == KIND_RAGGED_M && !Tr::kAnyGather) {
+                if (p.swiglu_h && orow) {
+                    hrow = p.swiglu_h + dest * p.ld_h;
+#pragma unroll
+                    for (int j = 0; j < kHAhead; ++j) load_h(ti.n0 + j * 16, hq[j]);
+                }
+            }
             const uint32_t buf = acc_count & 1u;
             const uint32_t acc_phase = (acc_count >> 1) & 1u;
             if (!warp_wait(&ctl->tmem_full[buf], acc_phase, abort_flag, p.status, 64, PAIR)) break;
@@ -880,7 +900,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 // each 8-H group gives 4 (gate, up) gradient pairs.  The H rows of
                 // this CTA's next tile are prefetched into L2 now (that epilogue
                 // runs a whole main loop later), and each step's 32 H values are
-                // loaded one step ahead, so the stores do not wait on DRAM.
+                // loaded kHAhead steps ahead (above), so the stores do not wait.
                 {
                     const int64_t tn = t + nslot;
                     if (tn < total_tiles) {
@@ -892,21 +912,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         }
                     }
                 }
-                const uint16_t* hrow = orow ? p.swiglu_h + dest * p.ld_h : nullptr;
-                auto load_h = [&](int col0, uint4 (&h)[4]) {
-                    if (hrow) {
-#pragma unroll
-                        for (int qd = 0; qd < 4; ++qd)
-                            if (col0 + qd * 4 < ncols)
-                                h[qd] = __ldg(reinterpret_cast<const uint4*>(hrow + 2 * col0 + qd * 8));
-                    }
-                };
-                uint4 hv[4], hnext[4];
-                load_h(ti.n0, hv);
+                // groups of kHAhead steps: the ring slot is a compile-time index and
+                // the loop body stays small (the whole 16-step loop unrolled ran
+                // twice as slow)
 #pragma unroll 1
-                for (int c = 0; c < kBN / 16; ++c) {
+                for (int cg = 0; cg < kBN / 16; cg += kHAhead)
+#pragma unroll
+                for (int j = 0; j < kHAhead; ++j) {
+                    const int c = cg + j;
                     const int col0 = ti.n0 + c * 16;
-                    if (c + 1 < kBN / 16) load_h(col0 + 16, hnext);
+                    uint4 (&hv)[4] = hq[j];
                     uint32_t v[16];
                     tmem_ld_32x32b_x16(taddr0 + c * 16, v);
                     tmem_ld_wait();
@@ -927,9 +942,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                                 st_global_16_policy(orow + 2 * col0 + qd * 8, make_uint4(o[0], o[1], o[2], o[3]), out_pol);
                             }
                         }
+                        // this slot's next use is kHAhead steps on
+                        if (c + kHAhead < kBN / 16) load_h(col0 + kHAhead * 16, hq[j]);
                     }
-#pragma unroll
-                    for (int qd = 0; qd < 4; ++qd) hv[qd] = hnext[qd];
                 }
                 ++acc_count;
                 continue;
