@@ -669,6 +669,16 @@ def run_suite(args):
     bf = torch.bfloat16
     peaks, src_kind = _peaks()
     tflops_sus = _peak_value(peaks, ["bf16_tflops_sustained", "bf16_tflops"], 1700.0)
+    hbm_gbs = _peak_value(peaks, ["hbm_gbs", "hbm_GBs", "hbm"], 6800.0)
+
+    def entry(ms, flops, nbytes):
+        # per-pass roofline: algorithmic bytes (operands read once, outputs written
+        # once), arithmetic intensity, and the cap min(tensor peak, AI x HBM)
+        tf = flops / (ms * 1e-3) / 1e12
+        ai = flops / nbytes
+        cap = min(tflops_sus, ai * hbm_gbs / 1e3)
+        return {"ms": ms, "tflops": tf, "bytes": nbytes, "flop_per_byte": ai, "cap_tflops": cap,
+                "frac_of_cap": tf / cap}
 
     def rnd(*shape, std=0.02):
         return (torch.randn(*shape, device=dev, generator=gen) * std).to(bf)
@@ -693,30 +703,33 @@ def run_suite(args):
         hist = m.cpu().numpy()
         Xp, W1, dH = rnd(R, K), rnd(E, N1, K), rnd(R, N1)
         H = torch.empty(R, N1, dtype=bf, device=dev)
+        # bytes: GEMM operands and output (bf16); dX1 adds its top-k token sum (R rows
+        # read, T rows written)
+        g1 = 2.0 * (R * K + E * N1 * K + R * N1)
         passes = {
-            "fwd1": (lambda: gg.forward(Xp, W1, m, gi, None, k, False, False, False, out=H), 2.0 * R * N1 * K),
-            "dX1": (lambda: gg.backward_dX(dH, W1, m, gi, T, k, True, False, token_sum=True), 2.0 * R * N1 * K),
-            "dW1": (lambda: gg.backward_dW(Xp, dH, m, gi, T, k, False, False), 2.0 * R * N1 * K),
+            "fwd1": (lambda: gg.forward(Xp, W1, m, gi, None, k, False, False, False, out=H), 2.0 * R * N1 * K, g1),
+            "dX1": (lambda: gg.backward_dX(dH, W1, m, gi, T, k, True, False, token_sum=True), 2.0 * R * N1 * K,
+                    g1 + 2.0 * (R * K + T * K)),
+            "dW1": (lambda: gg.backward_dW(Xp, dH, m, gi, T, k, False, False), 2.0 * R * N1 * K, g1),
         }
         res = {}
-        for name, (fn, fl) in passes.items():
-            ms = timed(fn)
-            res[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}
+        for name, (fn, fl, nb) in passes.items():
+            res[name] = entry(timed(fn), fl, nb)
         del Xp, W1, dH, H
         if I:
             A2, W2, dYp = rnd(R, I), rnd(E, K, I), rnd(R, K)
             fl = 2.0 * R * K * I
+            g2 = 2.0 * (R * I + E * K * I + R * K)
             for name, fn in (("fwd2", lambda: gg.forward(A2, W2, m, gi, None, k, False, True, False)),
                              ("dX2", lambda: gg.backward_dX(dYp, W2, m, gi, T, k, False, False)),
                              ("dW2", lambda: gg.backward_dW(A2, dYp, m, gi, T, k, False, False))):
-                ms = timed(fn)
-                res[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}
+                res[name] = entry(timed(fn), fl, g2)
             del A2, W2, dYp
         tot_ms = sum(v["ms"] for v in res.values())
         tot_fl = 3.0 * (2.0 * R * N1 * K + (2.0 * R * K * I if I else 0.0))
         print(json.dumps({"suite": cfg.name, "passes": res, "gemm_tflops": tot_fl / (tot_ms * 1e-3) / 1e12,
                           "frac_of_sustained_peak": tot_fl / (tot_ms * 1e-3) / 1e12 / tflops_sus,
-                          "peak_source": src_kind, "experts_empty": int((hist == 0).sum()),
+                          "peak_source": src_kind, "hbm_gbs": hbm_gbs, "experts_empty": int((hist == 0).sum()),
                           "largest_expert_share": float(hist.max() / hist.sum())}), flush=True)
         torch.cuda.empty_cache()
 
