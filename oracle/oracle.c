@@ -82,7 +82,7 @@ void oracle_widen_bf16(const uint16_t* in, int64_t n, double* out) {
  * ids[f], f = t*topk + j, is the expert chosen in slot j of token t.
  *   m_sizes[e]        = #{f : ids[f] == e}                 ([U] m_sizes, [V] expt_hist)
  *   offsets[e]        = sum_{e' < e} m_sizes[e'],  offsets[E] = R = T*topk
- *   padded_offsets    = the same prefix over ceil(m_e/b)*b  ([V] ragged-dw example, "if padded")
+ *   padded_offsets    = the same prefix over ceil(m_e/b)*b  ([V] ragged-dw example, its padded case)
  *   gather_idx[i]     = the flat slot f held by expert-order row i.  Rows of
  *                       expert e are offsets[e] .. offsets[e+1]-1 and hold its
  *                       slots in ascending f (stable counting sort; the pages
