@@ -288,6 +288,7 @@ SHAPES = [
     (200, 2, 5, 320, 264, (3,)),
     (64, 2, 4, 128, 256, ()),
     (513, 4, 9, 136, 520, (0, 8)),
+    (300, 2, 1, 136, 264, ()),  # one expert takes every slot: 5 row tiles, a phantom pair half
 ]
 FWD_FLAGS = [(px, py, fm) for px, py, fm in itertools.product([0, 1], [0, 1], [0, 1]) if not (fm and not py)]
 
@@ -456,7 +457,7 @@ def test_swiglu_bwd(rows, I):
 # 2-CTA pairs beyond: (1032, 520, 136, 4104, 776) has 173 tiles, odd m-tile counts
 # (a phantom pair half in both problems) and partial n-tiles.
 @pytest.mark.parametrize("dims", [(136, 72, 200, 264, 512), (512, 256, 1024, 2048, 4096), (8, 0, 64, 8, 16),
-                                  (1032, 520, 136, 4104, 776)])
+                                  (1032, 520, 136, 4104, 776), (1032, 0, 136, 4104, 776)])
 def test_dual_asym(ta, tb, dims):
     m0, m1, k, n0, n1 = dims
     cfg = synth.DualConfig(m0=m0, m1=m1, k=k, n0=n0, n1=n1, seed=7)
