@@ -296,7 +296,9 @@ FWD_FLAGS = [(px, py, fm) for px, py, fm in itertools.product([0, 1], [0, 1], [0
 def _problem(T, topk, E, K, N, empty, seed):
     ids = _ids(T, topk, E, seed, empty)
     rng = np.random.default_rng(seed)
-    _, w = synth.topk_softmax_route(rng.standard_normal((T, E)), topk)
+    # routing weights [T, topk] (with fewer experts than topk the draws repeat an
+    # expert, so the weights come from topk stand-in logits)
+    _, w = synth.topk_softmax_route(rng.standard_normal((T, max(E, topk))), topk)
     ro = orc.route(ids, T, topk, E)
     return ids, w, ro
 
@@ -469,6 +471,20 @@ def test_dual_asym(ta, tb, dims):
     R0, R1 = orc.dual_asym(d["X0"], d["X1"], d["W0"], d["W1"], bool(ta), bool(tb))
     assert_close(hbf(Y0), R0, "dual Y0")
     assert_close(hbf(Y1), R1, "dual Y1")
+
+
+def test_topk_weights_of_the_wrong_size_are_refused():
+    """The C ABI takes a bare pointer to [T, topk] weights; the binding refuses a
+    tensor of another size before anything is launched."""
+    T, topk, E, K, N = 16, 2, 3, 64, 64
+    X = dbf(synth.normal_bf16(1, "bw", (T * topk, K), 0.1))
+    W = dbf(synth.normal_bf16(2, "bw", (E, N, K), 0.1))
+    r = _route_gpu(_ids(T, topk, E, 5), E)
+    short = torch.ones(T, 1, dtype=torch.float32, device="cuda:0")
+    with pytest.raises(ValueError):
+        gg.forward(X, W, r["m_sizes"], r["gather_idx"], short, topk, False, True, True)
+    with pytest.raises(ValueError):
+        gg.forward_combine(X, W, r["m_sizes"], r["gather_idx"], short, topk)
 
 
 def test_forward_bad_sizes_sets_status():

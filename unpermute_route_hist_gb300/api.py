@@ -132,6 +132,8 @@ def forward(X, W, m_sizes, gather_idx, topk_w, topk: int, permute_x=False, permu
         raise ValueError("X must have T*topk rows without permute_x")
     _opt(gather_idx, torch.int32, "gather_idx", (R,))
     _opt(topk_w, torch.float32, "topk_w")
+    if topk_w is not None and topk_w.numel() != R:
+        raise ValueError("topk_w must have T*topk elements")
     Y = _out(out, (R, N), torch.bfloat16, X.device, "out")
     rc = _lib.load().gg_forward(_p(X), _p(W), _p(m_sizes), _p(gather_idx), _p(topk_w), T, topk, E, N,
                                 K, int(permute_x), int(permute_y), int(fuse_mul_post), _p(Y),
@@ -155,6 +157,8 @@ def forward_combine(X, W, m_sizes, gather_idx, topk_w, topk: int, permute_x=Fals
         raise ValueError("X must have T*topk rows without permute_x")
     _need(gather_idx, torch.int32, "gather_idx", (R,))
     _opt(topk_w, torch.float32, "topk_w")
+    if topk_w is not None and topk_w.numel() != R:
+        raise ValueError("topk_w must have T*topk elements")
     out = _out(out, (T, N), torch.bfloat16, X.device, "out")
     rc = _lib.load().gg_forward_combine(_p(X), _p(W), _p(m_sizes), _p(gather_idx), _p(topk_w), T, topk,
                                         E, N, K, int(permute_x), _p(out), _p(status), _stream(X.device))
