@@ -176,6 +176,8 @@ def forward_swiglu(X, W, m_sizes, gather_idx, topk: int, permute_x=False, *, sto
     rows = X.shape[0]
     T = rows if permute_x else rows // topk
     R = T * topk
+    if not permute_x and rows != R:
+        raise ValueError("X must have T*topk rows without permute_x")
     _opt(gather_idx, torch.int32, "gather_idx", (R,))
     Y = _out(out, (R, N), torch.bfloat16, X.device, "out") if store_y else None
     A = _out(out_act, (R, N // 2), torch.bfloat16, X.device, "out_act")
