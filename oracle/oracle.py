@@ -159,11 +159,22 @@ def permute(X, gather_idx, topk: int) -> np.ndarray:
     return Xp
 
 
+def _weights(topk_w, R: int):
+    """The [T, topk] routing weights as contiguous fp32, or None; the C oracle
+    reads R = T * topk of them, so any other size is refused here."""
+    if topk_w is None:
+        return None
+    w = _c(topk_w, np.float32)
+    if w.size != R:
+        raise ValueError("topk_w must have T*topk = %d elements, got %d" % (R, w.size))
+    return w
+
+
 def unpermute_combine(Y, row_id_map, topk_w, T: int, topk: int) -> np.ndarray:
     Y = _c(Y, np.uint16)
     N = Y.shape[1]
     rim = None if row_id_map is None else _c(row_id_map, np.int32)
-    w = None if topk_w is None else _c(topk_w, np.float32)
+    w = _weights(topk_w, T * topk)
     out = np.empty((T, N), np.float64)
     _load().oracle_unpermute_combine(Y, _ptr(rim), _ptr(w), T, topk, N, out)
     return out
@@ -176,7 +187,7 @@ def unpermute_combine_bwd(G, Y, row_id_map, topk_w, T: int, topk: int, want_dw: 
     R = T * topk
     Yc = None if (Y is None or not want_dw) else _c(Y, np.uint16)
     rim = None if row_id_map is None else _c(row_id_map, np.int32)
-    w = None if topk_w is None else _c(topk_w, np.float32)
+    w = _weights(topk_w, T * topk)
     dY = np.empty((R, N), np.float64)
     dw = np.empty((T, topk), np.float64) if want_dw else None
     _load().oracle_unpermute_combine_bwd(G, _ptr(Yc), _ptr(rim), _ptr(w), T, topk, N, dY, _ptr(dw))
@@ -223,7 +234,7 @@ def forward(X, W, m_sizes, gather_idx, topk_w, T, topk, permute_x, permute_y, fu
     E, N, K = W.shape
     m = _c(m_sizes, np.int32)
     g = None if gather_idx is None else _c(gather_idx, np.int32)
-    w = None if topk_w is None else _c(topk_w, np.float32)
+    w = _weights(topk_w, T * topk)
     Y = np.zeros((T * topk, N), np.float64)
     _load().oracle_forward(X, W, m, _ptr(g), _ptr(w), T, topk, E, N, K, int(permute_x),
                            int(permute_y), int(fuse_mul_post), Y)
@@ -254,7 +265,7 @@ def forward_rows(X, W, m_sizes, gather_idx, topk_w, topk, permute_x, permute_y, 
     E, N, K = W.shape
     m = _c(m_sizes, np.int32)
     g = None if gather_idx is None else _c(gather_idx, np.int32)
-    w = None if topk_w is None else _c(topk_w, np.float32)
+    w = _weights(topk_w, int(m.sum()))
     rows = _c(rows, np.int64)
     out = np.empty((rows.size, N), np.float64)
     dest = np.empty(rows.size, np.int64)
