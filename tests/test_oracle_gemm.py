@@ -291,3 +291,23 @@ def test_backward_dX_swiglu_matches_autograd(py):
     act = torch.nn.functional.silu(Ht[:, 0::2]) * Ht[:, 1::2]
     (act * dA).sum().backward()
     np.testing.assert_allclose(dH, Ht.grad.numpy(), rtol=1e-11, atol=1e-11)
+
+
+def test_weights_of_the_wrong_size_are_refused():
+    """The C oracle reads T*topk routing weights; the harness refuses any other
+    size instead of letting it read past the array."""
+    T, topk, E, K, N = 6, 2, 3, 8, 8
+    rng = np.random.default_rng(3)
+    ids = rng.integers(0, E, size=(T, topk)).astype(np.int32)
+    ro = orc.route(ids, T, topk, E)
+    X = synth.normal_bf16(1, "ww", (T * topk, K), 0.5)
+    W = synth.normal_bf16(2, "ww", (E, N, K), 0.5)
+    short = np.ones((T, 1), np.float32)
+    with pytest.raises(ValueError):
+        orc.forward(X, W, ro["m_sizes"], ro["gather_idx"], short, T, topk, 0, 1, 1)
+    with pytest.raises(ValueError):
+        orc.forward_rows(X, W, ro["m_sizes"], ro["gather_idx"], short, topk, 0, 1, 1, np.arange(4))
+    with pytest.raises(ValueError):
+        orc.unpermute_combine(X, ro["row_id_map"], short, T, topk)
+    ok = np.full((T, topk), 0.5, np.float32)
+    orc.forward(X, W, ro["m_sizes"], ro["gather_idx"], ok, T, topk, 0, 1, 1)
