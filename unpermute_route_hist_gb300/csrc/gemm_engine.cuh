@@ -585,9 +585,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 uint32_t tail_uses = 0;  // PAIR dW: tail blocks consumed so far
                 uint32_t acc_count = 0;
                 bool ok = true, any_mma = false;
+                // The next tile is decoded right after this tile's first MMAs are
+                // issued, while the tensor core works on them, instead of at the
+                // tile boundary, where the issuer may be the critical path.
+                TileInfo ti_next = slot < total_tiles ? decode_tile<KIND, PAIR>(slot, p, s_off, s_tp, rank) : TileInfo{};
                 for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
-                    const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
-                    if (ti.nkb == 0) continue;
+                    const TileInfo ti = ti_next;
+                    bool next_decoded = false;
+                    auto decode_next = [&]() {
+                        if (next_decoded) return;
+                        next_decoded = true;
+                        if (t + nslot < total_tiles) ti_next = decode_tile<KIND, PAIR>(t + nslot, p, s_off, s_tp, rank);
+                    };
+                    if (ti.nkb == 0) { decode_next(); continue; }
                     const uint32_t buf = acc_count & 1u;
                     const uint32_t acc_phase = (acc_count >> 1) & 1u;
                     if (!mbar_wait(&ctl->tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.status, 0, kWaitLimitNs, PAIR)) {
@@ -601,8 +611,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     // no tail test: the issue latency after a stage lands is the
                     // critical path
                     const int nfull = Tr::kTailBuf ? static_cast<int>(ti.red_len / kBK) : ti.nkb;
-                    for (int kb = 0; kb < nfull; ++kb) {
-                        if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+                    // one reduction block: wait for it, issue its MMAs, release its stage
+                    auto issue_block = [&](int kb) -> bool {
+                        if (!mbar_wait(&ctl->full[stage], phase, abort_flag, p.status)) return false;
                         tc_fence_after();
                         // cp.async writes are generic-proxy; order them before the
                         // tensor core's async-proxy reads of this stage
@@ -620,7 +631,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         else umma_commit(&ctl->empty[stage]);
                         any_mma = true;
                         if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                        return true;
+                    };
+                    // the first block is peeled off, so the per-block loop has no test
+                    // for the decode
+                    if (nfull > 0) {
+                        if (!issue_block(0)) { ok = false; break; }
+                        decode_next();
                     }
+                    for (int kb = 1; kb < nfull; ++kb)
+                        if (!issue_block(kb)) { ok = false; break; }
                     if (!ok) break;
                     if constexpr (Tr::kTailBuf) if (nfull < ti.nkb) {
                         // both CTAs' halves of the tail block have landed and were zeroed
@@ -640,6 +660,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         umma_commit_pair(&ctl->tempty, 0x3);  // the tail buffer is free in both CTAs
                         any_mma = true;
                     }
+                    decode_next();  // (a tile of only a tail block has not decoded it yet)
                     if (PAIR) umma_commit_pair(&ctl->tmem_full[buf], 0x3);
                     else umma_commit(&ctl->tmem_full[buf]);
                     ++acc_count;
