@@ -164,6 +164,51 @@ def oracle_sample(cfg, host, ro, rows_per_pass, rng):
     return dt, flops, desc
 
 
+def oracle_other_workloads():
+    """The oracle timed on the other workloads: the tiny layer in full (forward
+    with every flag, dX and dW of both GEMMs), the dual GEMM at its stated shape
+    in full, and the zipf64 forward on a row sample (its 1.1 TFLOP in full would
+    take about half a minute on the host).  TFLOP/s of what each computed."""
+    from oracle import oracle as orc
+    from unpermute_route_hist_gb300 import synth
+    res = {}
+    c = synth.TINY
+    ids, w = synth.route_choices(c)
+    t = synth.moe_tensors(c, ("X", "W1", "W2", "A2", "dH", "dY2"))
+    t0 = time.perf_counter()
+    ro = orc.route(ids, c.T, c.topk, c.E)
+    m, gi = ro["m_sizes"], ro["gather_idx"]
+    orc.forward(t["X"], t["W1"], m, gi, w, c.T, c.topk, 1, 1, 1)
+    orc.forward(t["A2"], t["W2"], m, gi, w, c.T, c.topk, 0, 1, 1)
+    orc.backward_dX(t["dH"], t["W1"], m, gi, c.T, c.topk, 1, 0)
+    orc.backward_dW(t["X"], t["dH"], m, gi, c.T, c.topk, 1, 0)
+    orc.backward_dX(t["dY2"], t["W2"], m, gi, c.T, c.topk, 0, 1)
+    orc.backward_dW(t["A2"], t["dY2"], m, gi, c.T, c.topk, 0, 1)
+    dt = time.perf_counter() - t0
+    fl = 3.0 * (2.0 * c.R * c.N1 * c.K + 2.0 * c.R * c.K * c.I)
+    res["tiny"] = {"seconds": dt, "tflops": fl / dt / 1e12, "sample": "full: route, both GEMMs' forward, dX and dW"}
+    d = synth.DUAL
+    dt_ = synth.dual_tensors(d)
+    t0 = time.perf_counter()
+    orc.dual_asym(dt_["X0"], dt_["X1"], dt_["W0"], dt_["W1"])
+    dt = time.perf_counter() - t0
+    fl = 2.0 * d.k * (d.m0 * d.n0 + d.m1 * d.n1)
+    res["dual"] = {"seconds": dt, "tflops": fl / dt / 1e12, "sample": "full, stated shape"}
+    c = synth.ZIPF64
+    ids, w = synth.route_choices(c)
+    t = synth.moe_tensors(c, ("X", "W1"))
+    ro = orc.route(ids, c.T, c.topk, c.E)
+    rows = np.sort(np.random.default_rng(3).choice(c.R, size=2048, replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    orc.forward_rows(t["X"], t["W1"], ro["m_sizes"], ro["gather_idx"], None, c.topk, 1, 0, 0, rows)
+    dt = time.perf_counter() - t0
+    fl = rows.size * 2.0 * c.N1 * c.K
+    res["zipf64_forward"] = {"seconds": dt, "tflops": fl / dt / 1e12,
+                             "sample": "%d of %d expert-order rows (full forward: about %.0f s at this rate)"
+                                       % (rows.size, c.R, 2.0 * c.R * c.N1 * c.K / (fl / dt))}
+    return res
+
+
 def make_host(cfg, which=("X", "W1", "W2", "G")):
     from unpermute_route_hist_gb300 import synth
     ids, w = synth.route_choices(cfg)
@@ -451,14 +496,18 @@ def run_gg(args, cfg):
             res_host[b][1].copy_(resd[b]["dXt"], non_blocking=True)
             d2h_ev[b].record(copy_stream)
 
-    def e2e_run(n):
+    def e2e_run(n, cevs=None):
         upload(0)
         for i in range(n):
             b = i % 2
             stream.wait_event(h2d_ev[b])
             if i >= 2:
                 stream.wait_event(d2h_ev[b])  # buffer b's results of step i-2 read back
+            if cevs is not None:
+                cevs[i][0].record(stream)
             step(srcs[b], res=resd[b])
+            if cevs is not None:
+                cevs[i][1].record(stream)
             comp_ev[b].record(stream)
             if i + 1 < n:
                 if i >= 1:
@@ -471,10 +520,19 @@ def run_gg(args, cfg):
     if ws > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # compute-stream events around each step: their sum is the GPU's compute time,
+    # the rest of the region is time the compute stream waited for copies
+    cevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(e_steps)]
+    e_clocks = Clocks(local)
+    e_clocks.start()
+    time.sleep(0.3)
     e0.record(copy_stream)
-    e2e_run(e_steps)
+    e2e_run(e_steps, cevs)
     e1.record(copy_stream)
     torch.cuda.synchronize()
+    e_clk = e_clocks.stop()
+    e_compute_ms = sum(a.elapsed_time(b) for a, b in cevs) / e_steps
     e_ms, e_value = aggregate_step_time(e0.elapsed_time(e1) / e_steps, step_flops, ws,
                                         dist if ws > 1 else None, dev)
     if not (torch.equal(res_host[0][0], res_host[1][0]) and torch.equal(res_host[0][1], res_host[1][1])):
@@ -562,10 +620,13 @@ def run_gg(args, cfg):
                            "route_ms": per["route"]},
             "variants": variants,
             "e2e": {"value": e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms},
+                    "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms,
+                    "compute_ms_per_step": e_compute_ms, "steps": e_steps, "clocks": e_clk},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
+        if not args.no_suite:
+            line["suite"] = measure_suite(dev, tflops_sus, hbm, src_kind)
         if not args.no_cpu_baseline and ws == 1:
             from oracle import oracle as orc
             orc.build()
@@ -575,7 +636,7 @@ def run_gg(args, cfg):
             dt, fl, desc = oracle_sample(cfg, host, ro, args.cpu_rows, rng)
             line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s",
                                     "cores": orc.num_threads(), "kind": "oracle", "sample": desc,
-                                    "seconds": dt}
+                                    "seconds": dt, "other_workloads": oracle_other_workloads()}
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -650,26 +711,27 @@ def run_only(args, cfg):
           flush=True)
 
 
-def run_suite(args):
-    """Diagnostic timings of the workloads the benchmark step does not cover:
-    the GEMM passes of fine128 (E=128, top-8, empty and near-empty experts) and
-    zipf64 (skewed routing), the dual GEMM at its stated shape and over a
-    sweep of (m0, m1).  Operands that the step would compute are seeded random
-    stand-ins; routing is each config's.  One JSON line per workload."""
+def measure_suite(dev, tflops_sus, hbm_gbs, src_kind):
+    """The workloads the layer step does not cover, timed on the device:
+      fine128 (E=128, top-8, empty and near-empty experts) and zipf64 (skewed
+      routing): every GEMM pass of the config on its own routing (operands that
+      a layer step would compute are seeded stand-ins of the same shape), and
+      the permute and combine row movers; all operands exceed L2;
+      dual: the two-expert GEMM at its stated shape and over the (m0, m1) sweep,
+      each rep preceded by a write of a buffer twice the L2 size, so operands
+      come from HBM.
+    Returns a dict (the bench line's "suite")."""
     import torch
 
     import unpermute_route_hist_gb300 as gg
-    from unpermute_route_hist_gb300 import _lib, synth
+    from unpermute_route_hist_gb300 import synth
 
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    _lib.load()
     gen = torch.Generator(device=dev)
     gen.manual_seed(11)
     bf = torch.bfloat16
-    peaks, src_kind = _peaks()
-    tflops_sus = _peak_value(peaks, ["bf16_tflops_sustained", "bf16_tflops"], 1700.0)
-    hbm_gbs = _peak_value(peaks, ["hbm_gbs", "hbm_GBs", "hbm"], 6800.0)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
 
     def entry(ms, flops, nbytes):
         # per-pass roofline: algorithmic bytes (operands read once, outputs written
@@ -684,25 +746,52 @@ def run_suite(args):
         return (torch.randn(*shape, device=dev, generator=gen) * std).to(bf)
 
     def timed(fn, reps=10):
+        # back-to-back reps; every operand here is larger than L2
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
+        a.record(stream)
         for _ in range(reps):
             fn()
-        b.record()
+        b.record(stream)
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps
 
+    def timed_flushed(fn, reps=20):
+        # median of reps, each after an L2-sized write; the flush keeps the GPU
+        # busy while the host enqueues the timed call, so no launch gap is timed
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            flush_buf.fill_(1)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    out = {"peak_tflops": tflops_sus, "hbm_gbs": hbm_gbs, "peak_source": src_kind + " bf16 sustained"}
     for cfg in (synth.FINE128, synth.ZIPF64):
         T, k, E, K, N1, I, R = cfg.T, cfg.topk, cfg.E, cfg.K, cfg.N1, cfg.I, cfg.R
-        ids, _ = synth.route_choices(cfg)
-        r = gg.route_hist_offsets(torch.from_numpy(ids).to(dev), E)
-        m, gi = r["m_sizes"], r["gather_idx"]
+        ids_np, w_np = synth.route_choices(cfg)
+        ids, wts = torch.from_numpy(ids_np).to(dev), torch.from_numpy(w_np).to(dev)
+        r = gg.route_hist_offsets(ids, E)
+        m, gi, rim = r["m_sizes"], r["gather_idx"], r["row_id_map"]
         hist = m.cpu().numpy()
-        Xp, W1, dH = rnd(R, K), rnd(E, N1, K), rnd(R, N1)
+        X = rnd(T, K)
+        Xp = gg.permute(X, rim, k)
+        W1, dH = rnd(E, N1, K), rnd(R, N1)
         H = torch.empty(R, N1, dtype=bf, device=dev)
+        res = {}
+        # row movers: GB/s of algorithmic bytes
+        perm_b = T * K * 2 + R * K * 2 + R * 4
+        ms = timed(lambda: gg.permute(X, rim, k, out=Xp))
+        res["permute"] = {"ms": ms, "GBps": perm_b / (ms * 1e-3) / 1e9,
+                          "frac_of_hbm": perm_b / (ms * 1e-3) / 1e9 / hbm_gbs}
         # bytes: GEMM operands and output (bf16); dX1 adds its top-k token sum (R rows
         # read, T rows written)
         g1 = 2.0 * (R * K + E * N1 * K + R * N1)
@@ -712,45 +801,37 @@ def run_suite(args):
                     g1 + 2.0 * (R * K + T * K)),
             "dW1": (lambda: gg.backward_dW(Xp, dH, m, gi, T, k, False, False), 2.0 * R * N1 * K, g1),
         }
-        res = {}
         for name, (fn, fl, nb) in passes.items():
             res[name] = entry(timed(fn), fl, nb)
         del Xp, W1, dH, H
         if I:
             A2, W2, dYp = rnd(R, I), rnd(E, K, I), rnd(R, K)
+            Y2 = torch.empty(R, K, dtype=bf, device=dev)
             fl = 2.0 * R * K * I
             g2 = 2.0 * (R * I + E * K * I + R * K)
-            for name, fn in (("fwd2", lambda: gg.forward(A2, W2, m, gi, None, k, False, True, False)),
+            for name, fn in (("fwd2", lambda: gg.forward(A2, W2, m, gi, None, k, False, True, False, out=Y2)),
                              ("dX2", lambda: gg.backward_dX(dYp, W2, m, gi, T, k, False, False)),
                              ("dW2", lambda: gg.backward_dW(A2, dYp, m, gi, T, k, False, False))):
                 res[name] = entry(timed(fn), fl, g2)
-            del A2, W2, dYp
-        tot_ms = sum(v["ms"] for v in res.values())
+            comb_b = R * K * 2 + R * 4 + R * 4 + T * K * 2
+            ms = timed(lambda: gg.unpermute_combine(Y2, None, wts, T, k, out=X))
+            res["combine"] = {"ms": ms, "GBps": comb_b / (ms * 1e-3) / 1e9,
+                              "frac_of_hbm": comb_b / (ms * 1e-3) / 1e9 / hbm_gbs}
+            del A2, W2, dYp, Y2
+        gemm = [n for n in res if "tflops" in res[n]]
+        tot_ms = sum(res[n]["ms"] for n in gemm)
         tot_fl = 3.0 * (2.0 * R * N1 * K + (2.0 * R * K * I if I else 0.0))
-        print(json.dumps({"suite": cfg.name, "passes": res, "gemm_tflops": tot_fl / (tot_ms * 1e-3) / 1e12,
-                          "frac_of_sustained_peak": tot_fl / (tot_ms * 1e-3) / 1e12 / tflops_sus,
-                          "peak_source": src_kind, "hbm_gbs": hbm_gbs, "experts_empty": int((hist == 0).sum()),
-                          "largest_expert_share": float(hist.max() / hist.sum())}), flush=True)
+        out[cfg.name] = {
+            "passes": res, "gemm_ms": tot_ms, "gemm_tflops": tot_fl / (tot_ms * 1e-3) / 1e12,
+            "frac_of_peak": tot_fl / (tot_ms * 1e-3) / 1e12 / tflops_sus,
+            "min_frac_of_cap": min(res[n]["frac_of_cap"] for n in gemm),
+            "experts_empty": int((hist == 0).sum()),
+            "largest_expert_share": float(hist.max() / hist.sum()),
+            "workload": "T=%d, K=%d, N1=%d, I=%d, E=%d, topk=%d, %s routing" % (T, K, N1, I, E, k, cfg.routing)}
+        del X, ids, wts, r, m, gi, rim
         torch.cuda.empty_cache()
 
-    # Dual GEMM: per call as issued from Python (host-bound for small shapes), and
-    # the device time of the same calls replayed from a captured CUDA graph.
-    def graph_ms(fn, reps=20):
-        fn()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(reps):
-                fn()
-        g.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps
-
+    # Dual GEMM: device time per call, L2 flushed before each rep.
     sweep = {}
     ms_list = [128, 256, 512, 1024, 2048, 4096, 8192]
     kd, n0, n1 = synth.DUAL.k, synth.DUAL.n0, synth.DUAL.n1
@@ -761,15 +842,35 @@ def run_suite(args):
             Y0 = torch.empty(m0, n0, dtype=bf, device=dev)
             Y1 = torch.empty(m1, n1, dtype=bf, device=dev)
             fn = lambda: gg.dual_asym(X0, X1, W0, W1, out0=Y0, out1=Y1)
-            ms = timed(fn)
-            gms = graph_ms(fn)
+            ms = timed_flushed(fn, reps=9 if (m0, m1) != (synth.DUAL.m0, synth.DUAL.m1) else 30)
             fl = 2.0 * kd * (m0 * n0 + m1 * n1)
-            sweep["%d,%d" % (m0, m1)] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
-                                         "graph_ms": gms, "graph_tflops": fl / (gms * 1e-3) / 1e12}
+            nb = 2.0 * (m0 * kd + m1 * kd + kd * n0 + kd * n1 + m0 * n0 + m1 * n1)
+            sweep["%d,%d" % (m0, m1)] = entry(ms, fl, nb)
+    del flush_buf
+    torch.cuda.empty_cache()
     base = sweep["%d,%d" % (synth.DUAL.m0, synth.DUAL.m1)]
-    print(json.dumps({"suite": "dual", "stated_shape": base, "sweep_m0_m1": sweep,
-                      "largest_graph_tflops": max(v["graph_tflops"] for v in sweep.values())}),
-          flush=True)
+    out["dual"] = {"stated_shape": base, "sweep_m0_m1": sweep,
+                   "largest_tflops": max(v["tflops"] for v in sweep.values()),
+                   "timing": "device events per call, median of reps, L2 flushed (2x L2 written) before each",
+                   "workload": "X0 [m0,%d] X1 [m1,%d] W0 [%d,%d] W1 [%d,%d], stated m0=%d m1=%d; sweep m0,m1 in %s"
+                               % (kd, kd, kd, n0, kd, n1, synth.DUAL.m0, synth.DUAL.m1, ms_list)}
+    return out
+
+
+def run_suite(args):
+    """--suite: the suite alone, one diagnostic JSON line (not the bench line)."""
+    import torch
+
+    from unpermute_route_hist_gb300 import _lib
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _lib.load()
+    peaks, src_kind = _peaks()
+    tflops_sus = _peak_value(peaks, ["bf16_tflops_sustained", "bf16_tflops"], 1700.0)
+    hbm_gbs = _peak_value(peaks, ["hbm_gbs", "hbm_GBs", "hbm"], 6800.0)
+    print(json.dumps({"suite": measure_suite(dev, tflops_sus, hbm_gbs, src_kind),
+                      "note": "diagnostic, not a bench line"}), flush=True)
 
 
 def main():
@@ -784,10 +885,12 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=640,
                     help="oracle rows per pass in the cpu_baseline sample (about 10 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-suite", action="store_true",
+                    help="leave fine128, zipf64 and the dual GEMM out of the bench line")
     ap.add_argument("--only", choices=["fwd1", "fwd2", "dX2", "dW2", "dX1", "dW1"],
                     help="time one GEMM pass alone on its own operands (for profiling)")
     ap.add_argument("--suite", action="store_true",
-                    help="time fine128, zipf64 and the dual GEMM (diagnostic lines, not the bench line)")
+                    help="time only fine128, zipf64 and the dual GEMM (a diagnostic line, not the bench line)")
     args = ap.parse_args()
     from unpermute_route_hist_gb300 import synth
     cfg = synth.CONFIGS[args.config]

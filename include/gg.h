@@ -116,10 +116,13 @@ int gg_route_hist_offsets(const int32_t* topk_ids, int64_t T, int topk, int E, i
  *  - The first call on each device looks up that array's device address
  *    (once per device, with that device current); make that first call
  *    before any stream capture.
- *  - All calls share the array: calls that overlap on the GPU race on it, so
- *    the caller must serialise them.  No state carries over between calls.
+ *  - Each device holds its own copy of the array, shared by every call on
+ *    that device: calls that overlap on the same device (concurrent streams)
+ *    race on it, so the caller must serialise them; calls on different
+ *    devices do not interfere.  No state carries over between calls.
  *  - A problem whose scratch, ceil(T*topk/256) * E * 4 bytes, exceeds the
- *    array returns GG_ERR_WORKSPACE without launching.
+ *    array returns GG_ERR_WORKSPACE without launching.  A device numbered 64
+ *    or higher returns GG_ERR_UNSUPPORTED.
  * Allocates nothing. */
 int gg_route_hist_offsets_noalloc(const int32_t* topk_ids, int64_t T, int topk, int E,
                                   int pad_block, int32_t* m_sizes, int32_t* offsets,

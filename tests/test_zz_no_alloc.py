@@ -5,8 +5,9 @@ that must not pay for an allocation).  It keeps the counting sort's scratch
 in a static device array instead of a caller workspace.
 
 Checked through the C ABI against gg_route_hist_offsets (which takes a
-workspace): two calls in a row on different routings must both give the same
-integers, bit for bit.  The file sorts last so that a stop-at-first-failure
+workspace) and against the CPU oracle's routing: two calls in a row on
+different routings must both give the same integers, bit for bit; so must a
+problem whose scratch is exactly the static array's size.  The file sorts last so that a stop-at-first-failure
 run has already run every other test; it also passes alone in a fresh
 process (it builds and loads the library itself)."""
 import ctypes
@@ -73,6 +74,36 @@ def test_noalloc_route_matches_workspace_route_twice(lib):
         assert int(st_n.item()) == 0 and int(st_w.item()) == 0
         for k in got:
             assert torch.equal(got[k], ref[k]), k
+        _check_against_oracle(got, ids_np, E, pad)
+
+
+def _check_against_oracle(got, ids_np, E, pad):
+    from oracle import oracle as orc
+    T, topk = ids_np.shape
+    ro = orc.route(ids_np, T, topk, E, pad_block=pad)
+    for k in ("m_sizes", "offsets", "padded_offsets", "gather_idx", "row_id_map"):
+        np.testing.assert_array_equal(got[k].cpu().numpy(), ro[k], err_msg=k)
+
+
+def test_noalloc_route_at_exactly_the_scratch_size(lib):
+    from unpermute_route_hist_gb300 import _lib
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    # ceil(65536/256) = 256 chunks * 1024 experts * 4 bytes = 1 MiB: the largest problem accepted
+    T, topk, E, pad = 65536, 1, 1024, 32
+    assert lib.gg_route_workspace_size(T, topk, E) == _lib.GG_ROUTE_NOALLOC_SCRATCH_BYTES
+    ids_np = np.random.default_rng(9).integers(0, E, size=(T, topk)).astype(np.int32)
+    ids = torch.from_numpy(ids_np).to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    got = _outs(T, topk, E)
+    assert _call_noalloc(lib, ids, T, topk, E, pad, got, st, stream) == _lib.GG_OK
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _check_against_oracle(got, ids_np, E, pad)
+    # one slot more needs a 257th chunk: refused on the host, nothing launched
+    fake = ctypes.c_void_p(4096)
+    assert lib.gg_route_hist_offsets_noalloc(fake, T + 1, 1, E, 0, fake, fake, None, fake, fake,
+                                             None, None) == _lib.GG_ERR_WORKSPACE
 
 
 def test_noalloc_route_rejects_problems_beyond_its_scratch(lib):

@@ -151,13 +151,6 @@ using namespace gg;
 namespace {
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
-int check_launch(int rc) {
-    if (rc != GG_OK) {
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) record_cuda_error(e);
-    }
-    return rc;
-}
 }  // namespace
 
 extern "C" {
@@ -203,9 +196,9 @@ int gg_route_hist_offsets(const int32_t* topk_ids, int64_t T, int topk, int E, i
     if (pad_block > 0 && !padded_offsets) return GG_ERR_INVALID_ARG;
     const size_t need = route_workspace_bytes(T, topk, E);
     if (R > 0 && (!workspace || workspace_bytes < need)) return GG_ERR_WORKSPACE;
-    return check_launch(route_launch(topk_ids, T, topk, E, pad_block, m_sizes, offsets,
-                                     padded_offsets, gather_idx, row_id_map,
-                                     static_cast<int32_t*>(workspace), status, as_stream(stream)));
+    return route_launch(topk_ids, T, topk, E, pad_block, m_sizes, offsets, padded_offsets,
+                        gather_idx, row_id_map, static_cast<int32_t*>(workspace), status,
+                        as_stream(stream));
 }
 
 int gg_permute(const gg_bf16* X, const int32_t* row_id_map, int64_t T, int topk, int64_t K,
@@ -216,7 +209,7 @@ int gg_permute(const gg_bf16* X, const int32_t* row_id_map, int64_t T, int topk,
     if (T == 0 || K == 0) return GG_OK;
     if (!X || !row_id_map || !Xp) return GG_ERR_INVALID_ARG;
     if (!al16(X) || !al16(Xp)) return GG_ERR_UNSUPPORTED;
-    return check_launch(permute_launch(X, row_id_map, T, topk, K, Xp, status, as_stream(stream)));
+    return permute_launch(X, row_id_map, T, topk, K, Xp, status, as_stream(stream));
 }
 
 int gg_unpermute_combine(const gg_bf16* Y, const int32_t* row_id_map, const float* topk_w,
@@ -228,8 +221,7 @@ int gg_unpermute_combine(const gg_bf16* Y, const int32_t* row_id_map, const floa
     if (T == 0 || N == 0) return GG_OK;
     if (!Y || !out) return GG_ERR_INVALID_ARG;
     if (!al16(Y) || !al16(out)) return GG_ERR_UNSUPPORTED;
-    return check_launch(
-        combine_launch(Y, row_id_map, topk_w, T, topk, N, out, status, as_stream(stream)));
+    return combine_launch(Y, row_id_map, topk_w, T, topk, N, out, status, as_stream(stream));
 }
 
 int gg_unpermute_combine_bwd(const gg_bf16* G, const gg_bf16* Y, const int32_t* row_id_map,
@@ -249,8 +241,8 @@ int gg_unpermute_combine_bwd(const gg_bf16* G, const gg_bf16* Y, const int32_t* 
     }
     if (!G || !dY) return GG_ERR_INVALID_ARG;
     if (!al16(G) || !al16(dY) || (Y && !al16(Y))) return GG_ERR_UNSUPPORTED;
-    return check_launch(combine_bwd_launch(G, dw ? Y : nullptr, row_id_map, topk_w, T, topk, N, dY,
-                                           dw, status, as_stream(stream)));
+    return combine_bwd_launch(G, dw ? Y : nullptr, row_id_map, topk_w, T, topk, N, dY, dw, status,
+                              as_stream(stream));
 }
 
 int gg_swiglu_bwd(const gg_bf16* H, const gg_bf16* dA, int64_t rows, int64_t I, gg_bf16* dH,
@@ -260,15 +252,14 @@ int gg_swiglu_bwd(const gg_bf16* H, const gg_bf16* dA, int64_t rows, int64_t I, 
     if (rows == 0 || I == 0) return GG_OK;
     if (!H || !dA || !dH) return GG_ERR_INVALID_ARG;
     if (!al16(H) || !al16(dA) || !al16(dH)) return GG_ERR_UNSUPPORTED;
-    return check_launch(swiglu_bwd_launch(H, dA, rows, I, dH, as_stream(stream)));
+    return swiglu_bwd_launch(H, dA, rows, I, dH, as_stream(stream));
 }
 
 int gg_selftest_bounded_wait(int32_t* status, int32_t* result, uint64_t limit_ns, void* stream) {
     if (!status || !result || limit_ns == 0 || limit_ns > kWaitLimitNs) return GG_ERR_INVALID_ARG;
+    clear_pending_launch_error();
     selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(status, limit_ns, result);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
-    return GG_OK;
+    return launch_result();
 }
 
 }  // extern "C"

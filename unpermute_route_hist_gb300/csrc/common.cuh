@@ -430,4 +430,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
+// ------------------------------------------------------------ host launch --
+
+void record_cuda_error(cudaError_t e);
+
+// Clear a non-sticky error that earlier work left pending on this host thread,
+// so that the check after this call's launches reports only its own launches.
+inline void clear_pending_launch_error() { (void)cudaGetLastError(); }
+
+// Status of the launches enqueued since the last clear: GG_OK, or GG_ERR_CUDA
+// with the error's text recorded (gg_last_cuda_error) before it is cleared.
+inline int launch_result() {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return GG_ERR_CUDA;
+    }
+    return GG_OK;
+}
+
+// Status of one runtime call (a memset): GG_OK, or GG_ERR_CUDA with its text.
+inline int cuda_result(cudaError_t e) {
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return GG_ERR_CUDA;
+    }
+    return GG_OK;
+}
+
 }  // namespace gg

@@ -1192,7 +1192,6 @@ bool encode_map_mn_chunks_planes(CUtensorMap* m, const void* base, uint64_t cols
                                  uint64_t plane_stride_elems, uint32_t box_rows,
                                  uint32_t box_chunks);
 int num_sms();
-void record_cuda_error(cudaError_t e);
 
 template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR>
 int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
@@ -1215,6 +1214,7 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
     }
     const int64_t sms = num_sms();
     if (tile_bound < 1) tile_bound = 1;
+    clear_pending_launch_error();
     if (!PAIR) {
         const int64_t grid = tile_bound < sms ? tile_bound : sms;
         kern<<<static_cast<unsigned>(grid), Tr::kThreads, smem, stream>>>(a0, b0, a1, b1, p);
@@ -1248,9 +1248,7 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
         e = cudaLaunchKernelEx(&cfg, kern, a0, b0, a1, b1, p);
         if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
     }
-    e = cudaGetLastError();
-    if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
-    return GG_OK;
+    return launch_result();
 }
 
 }  // namespace gg

@@ -271,10 +271,11 @@ unsigned move_grid(int64_t rows) {
 int permute_launch(const uint16_t* X, const int32_t* row_id_map, int64_t T, int topk, int64_t K,
                    uint16_t* Xp, int32_t* status, cudaStream_t stream) {
     const int64_t R = T * topk;
+    clear_pending_launch_error();
     permute_kernel<<<move_grid((T + kWarpsPerCta - 1) / kWarpsPerCta), kMoveThreads, 0, stream>>>(
         reinterpret_cast<const uint4*>(X), row_id_map, T, topk, K / 8, reinterpret_cast<uint4*>(Xp),
         R, status);
-    return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
+    return launch_result();
 }
 
 int swiglu_bwd_launch(const uint16_t* H, const uint16_t* dA, int64_t rows, int64_t I, uint16_t* dH,
@@ -283,29 +284,32 @@ int swiglu_bwd_launch(const uint16_t* H, const uint16_t* dA, int64_t rows, int64
     int64_t blocks = (groups + kMoveThreads - 1) / kMoveThreads;
     const int64_t cap = static_cast<int64_t>(move_grid(INT64_MAX)) * 4;
     if (blocks > cap) blocks = cap;
+    clear_pending_launch_error();
     swiglu_bwd_kernel<<<static_cast<unsigned>(blocks), kMoveThreads, 0, stream>>>(
         reinterpret_cast<const uint4*>(H), reinterpret_cast<const uint4*>(dA), groups,
         reinterpret_cast<uint4*>(dH));
-    return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
+    return launch_result();
 }
 
 int combine_bwd_launch(const uint16_t* G, const uint16_t* Y, const int32_t* row_id_map,
                        const float* topk_w, int64_t T, int topk, int64_t N, uint16_t* dY, float* dw,
                        int32_t* status, cudaStream_t stream) {
     const int64_t R = T * topk;
+    clear_pending_launch_error();
     combine_bwd_kernel<<<move_grid(T), kMoveThreads, 0, stream>>>(
         reinterpret_cast<const uint4*>(G), reinterpret_cast<const uint4*>(Y), row_id_map, topk_w, T,
         topk, N / 8, R, reinterpret_cast<uint4*>(dY), dw, status);
-    return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
+    return launch_result();
 }
 
 int combine_launch(const uint16_t* Y, const int32_t* row_id_map, const float* topk_w, int64_t T,
                    int topk, int64_t N, uint16_t* out, int32_t* status, cudaStream_t stream) {
     const int64_t R = T * topk;
+    clear_pending_launch_error();
     combine_kernel<<<move_grid((T + kWarpsPerCta - 1) / kWarpsPerCta), kMoveThreads, 0, stream>>>(
         reinterpret_cast<const uint4*>(Y), row_id_map, topk_w, T, topk, N / 8, R,
         reinterpret_cast<uint4*>(out), status);
-    return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
+    return launch_result();
 }
 
 }  // namespace gg

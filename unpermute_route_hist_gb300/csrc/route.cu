@@ -198,20 +198,22 @@ int route_launch(const int32_t* ids, int64_t T, int topk, int E, int pad_block, 
     const int64_t C = num_chunks(R);
     const size_t smem = static_cast<size_t>(kWarpsPerCta) * E * sizeof(int32_t);
     const unsigned grid_chunks = static_cast<unsigned>((C + kWarpsPerCta - 1) / kWarpsPerCta);
+    clear_pending_launch_error();
     // kWarpsPerCta * E * 4 bytes <= 32 KB for E <= GG_MAX_EXPERTS: default limit.
     if (R > 0) {
         route_count_kernel<<<grid_chunks, kWarpsPerCta * 32, smem, stream>>>(ids, R, E, C, counts,
                                                                             status);
         route_scan_kernel<<<E, 256, 0, stream>>>(counts, C, m_sizes);
     } else {
-        cudaMemsetAsync(m_sizes, 0, sizeof(int32_t) * E, stream);
+        const int rc = cuda_result(cudaMemsetAsync(m_sizes, 0, sizeof(int32_t) * E, stream));
+        if (rc != GG_OK) return rc;
     }
     route_offsets_kernel<<<1, 1024, 0, stream>>>(m_sizes, E, pad_block, R, offsets,
                                                  pad_block > 0 ? padded : nullptr, status);
     if (R > 0)
         route_scatter_kernel<<<grid_chunks, kWarpsPerCta * 32, smem, stream>>>(
             ids, R, E, C, counts, offsets, gather_idx, row_id_map);
-    return cudaGetLastError() == cudaSuccess ? GG_OK : GG_ERR_CUDA;
+    return launch_result();
 }
 
 size_t route_workspace_bytes(int64_t T, int topk, int E) {

@@ -9,11 +9,13 @@
 // fixed static device array of this library instead of a caller workspace.
 //
 // The array holds GG_ROUTE_NOALLOC_SCRATCH_BYTES bytes; every GPU that loads
-// the library keeps it until the process exits.  All calls share it: calls
-// that overlap on the GPU (concurrent streams, or devices racing on the same
-// array through peer access) race on it and must be serialised by the caller.
-// Nothing in it needs clearing between calls: the count pass writes every
-// entry the later passes read.
+// the library keeps its own copy until the process exits.  All calls on one
+// device share that device's copy: calls that overlap on the same device (on
+// concurrent streams) race on it and must be serialised by the caller; calls
+// on different devices do not interfere.  Devices numbered kMaxDevices (64) or
+// higher are refused with GG_ERR_UNSUPPORTED.  Nothing in the array needs
+// clearing between calls: the count pass writes every entry the later passes
+// read.
 #include <mutex>
 
 #include "common.cuh"
@@ -23,7 +25,6 @@ int route_launch(const int32_t* ids, int64_t T, int topk, int E, int pad_block, 
                  int32_t* offsets, int32_t* padded, int32_t* gather_idx, int32_t* row_id_map,
                  int32_t* counts, int32_t* status, cudaStream_t stream);
 size_t route_workspace_bytes(int64_t T, int topk, int E);
-void record_cuda_error(cudaError_t e);
 }  // namespace gg
 
 namespace {
@@ -78,12 +79,7 @@ extern "C" int gg_route_hist_offsets_noalloc(const int32_t* topk_ids, int64_t T,
     int32_t* scratch = nullptr;
     const int rc = scratch_for_current_device(&scratch);
     if (rc != GG_OK) return rc;
-    const int lrc = gg::route_launch(topk_ids, T, topk, E, pad_block, m_sizes, offsets,
-                                     padded_offsets, gather_idx, row_id_map, scratch, status,
-                                     reinterpret_cast<cudaStream_t>(stream));
-    if (lrc != GG_OK) {
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) gg::record_cuda_error(e);
-    }
-    return lrc;
+    return gg::route_launch(topk_ids, T, topk, E, pad_block, m_sizes, offsets, padded_offsets,
+                            gather_idx, row_id_map, scratch, status,
+                            reinterpret_cast<cudaStream_t>(stream));
 }
