@@ -550,6 +550,13 @@ def run_gg(args, cfg):
         return a.elapsed_time(b) / reps
 
     rr = o
+    # workspaces: the larger dW gather copy (dY2 rows, R x K; X rows are R x K too)
+    # and the fused combine's fp32 sums
+    dw_ws = torch.empty(max(gg.workspace_size(_lib.GG_OP_BACKWARD_DW, T, k, E, K, I, _lib.GG_PERMUTE_Y),
+                            gg.workspace_size(_lib.GG_OP_BACKWARD_DW, T, k, E, N1, K, _lib.GG_PERMUTE_X)),
+                        dtype=torch.uint8, device=dev)
+    comb_ws = torch.empty(gg.workspace_size(_lib.GG_OP_FORWARD_COMBINE, T, k, E, K, I), dtype=torch.uint8,
+                          device=dev)
     variants = {
         "fwd1_fused_token_gather": (time_call(lambda: gg.forward(
             src["X"], W1, rr["m_sizes"], rr["gather_idx"], None, k, True, False, False, out=H,
@@ -557,21 +564,34 @@ def run_gg(args, cfg):
         "dX2_fused_slot_gather": (time_call(lambda: gg.backward_dX(
             dY2, W2, rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dA2,
             status=status)), passes["dX2"]),
-        "dW2_fused_slot_gather": (time_call(lambda: gg.backward_dW(
+        # dW with the slot gather: rows copied into the workspace, then the dense
+        # reduction (the library's path when a workspace is given) ...
+        "dW2_slot_gather_via_workspace": (time_call(lambda: gg.backward_dW(
             A2, dY2, rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dW2,
-            status=status)), passes["dW2"]),
+            workspace=dw_ws, status=status)), passes["dW2"]),
+        # ... and fused into the reduction's operand loads (no workspace)
+        "dW2_slot_gather_fused_in_loads": (time_call(lambda: gg.backward_dW(
+            A2, dY2, rr["m_sizes"], rr["gather_idx"], T, k, False, True, out=dW2,
+            workspace=False, status=status)), passes["dW2"]),
         # inference form of GEMM2 + combine: the combine fused into the epilogue
-        # (atomic adds; the per-slot rows the training step keeps are not stored)
-        "fwd2_fused_combine": (time_call(lambda: gg.forward_combine(
+        # (atomic adds; the per-slot rows the training step keeps are not stored),
+        # summed in an fp32 workspace, or in bf16 in the output
+        "fwd2_fused_combine_fp32": (time_call(lambda: gg.forward_combine(
             A2, W2, rr["m_sizes"], rr["gather_idx"], src["w"], k, False, out=out,
-            status=status)), passes["fwd2"]),
+            workspace=comb_ws, status=status)), passes["fwd2"]),
+        "fwd2_fused_combine_bf16": (time_call(lambda: gg.forward_combine(
+            A2, W2, rr["m_sizes"], rr["gather_idx"], src["w"], k, False, out=out,
+            workspace=False, status=status)), passes["fwd2"]),
         # dX2 with the SwiGLU backward fused into its epilogue (no dA buffer); the
         # step runs dX2 then gg_swiglu_bwd, which measures faster
         "dX2_fused_swiglu_bwd": (time_call(lambda: gg.backward_dX_swiglu(
             dYp, W2, rr["m_sizes"], k, H, out=dH, status=status)), passes["dX2"]),
-        "dW1_fused_token_gather": (time_call(lambda: gg.backward_dW(
+        "dW1_token_gather_via_workspace": (time_call(lambda: gg.backward_dW(
             src["X"], dH, rr["m_sizes"], rr["gather_idx"], T, k, True, False, out=dW1,
-            status=status), reps=1), passes["dW1"]),
+            workspace=dw_ws, status=status)), passes["dW1"]),
+        "dW1_token_gather_fused_in_loads": (time_call(lambda: gg.backward_dW(
+            src["X"], dH, rr["m_sizes"], rr["gather_idx"], T, k, True, False, out=dW1,
+            workspace=False, status=status), reps=1), passes["dW1"]),
     }
     variants = {n: {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12} for n, (ms, fl) in variants.items()}
 

@@ -20,7 +20,13 @@
  *    atomic compare-and-swap from 0, to a GG_DEV_* code when they find bad
  *    input data (an expert id out of range, a row index out of range) or a
  *    bounded wait ran out.  The offending access is skipped, never performed.
- *    The caller zeroes it and reads it after synchronising.
+ *    The caller zeroes it and reads it after synchronising, or lets
+ *    gg_read_status do both (it maps the word to GG_ERR_DEVICE_CHECK or
+ *    GG_ERR_TIMEOUT).
+ *  - `workspace` (the entry points that take one): caller-owned device
+ *    scratch of at least gg_workspace_size() bytes for that call, 16-byte
+ *    aligned; no initialisation needed, contents garbage afterwards.  Too
+ *    small -> GG_ERR_WORKSPACE with nothing launched.
  *  - Size rules (else GG_ERR_UNSUPPORTED): row widths K and N multiples of 8
  *    (16-byte rows), every tensor pointer 16-byte aligned, E <= GG_MAX_EXPERTS,
  *    topk <= GG_MAX_TOPK, R < 2^31.
@@ -50,6 +56,8 @@ typedef uint16_t gg_bf16;
 #define GG_ERR_INVALID_ARG (-1)
 #define GG_ERR_UNSUPPORTED (-2)
 #define GG_ERR_CUDA (-3)
+#define GG_ERR_DEVICE_CHECK (-4) /* from gg_read_status: a kernel found bad input data */
+#define GG_ERR_TIMEOUT (-5)      /* from gg_read_status: a bounded wait in a kernel ran out */
 #define GG_ERR_WORKSPACE (-6)
 
 /* device status word codes */
@@ -62,6 +70,16 @@ typedef uint16_t gg_bf16;
 #define GG_MAX_EXPERTS 2048
 #define GG_MAX_TOPK 64
 #define GG_ROUTE_NOALLOC_SCRATCH_BYTES (1u << 20)
+/* gg_forward_combine without a workspace (bf16 accumulation) takes topk up to this */
+#define GG_COMBINE_BF16_MAX_TOPK 16
+
+/* operations for gg_workspace_size */
+#define GG_OP_ROUTE 1            /* gg_route_hist_offsets */
+#define GG_OP_BACKWARD_DW 2      /* gg_backward_dW with a gathered operand */
+#define GG_OP_FORWARD_COMBINE 3  /* gg_forward_combine, fp32 accumulation */
+/* flags for gg_workspace_size */
+#define GG_PERMUTE_X 1
+#define GG_PERMUTE_Y 2
 
 /* Human-readable text for a GG_* return code (static storage). */
 const char* gg_status_string(int code);
@@ -69,6 +87,20 @@ const char* gg_status_string(int code);
 const char* gg_device_status_string(int code);
 /* Text of the last CUDA error seen by a host call on this thread. */
 const char* gg_last_cuda_error(void);
+
+/* Bytes of workspace an entry point needs for this problem (0: it takes none,
+ * or needs none for these flags).  Same size arguments as the call (for a
+ * call without N or K pass 0); flags: GG_PERMUTE_X | GG_PERMUTE_Y as the
+ * call's permute flags.  No counterpart on the pages: the library allocates
+ * nothing, so every scratch buffer comes from the caller through this size. */
+size_t gg_workspace_size(int op, int64_t T, int topk, int E, int64_t N, int64_t K, int flags);
+
+/* Synchronises `stream`, reads the device status word `status` (device int32)
+ * and returns GG_OK when it is GG_DEV_OK, GG_ERR_TIMEOUT for GG_DEV_TIMEOUT,
+ * GG_ERR_DEVICE_CHECK for any other device code, GG_ERR_CUDA if the read
+ * fails.  *code (host int32, may be NULL) receives the GG_DEV_* code.  The
+ * word is left as it is.  No counterpart on the pages. */
+int gg_read_status(const int32_t* status, int32_t* code, void* stream);
 
 /* Diagnostic: runs, in one CTA, the bounded mbarrier wait that every
  * pipelined kernel of this library uses, on a barrier phase nothing ever
@@ -195,8 +227,15 @@ int gg_forward(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
  *   out[t] = sum over the slots f = t*topk + j of  w[f] * (a_f @ W[e(f)]^T)
  *   a_f, W[e] as gg_forward (permute_x selects X [T, K] with the gather, else
  *   X [R, K] in expert order); w = topk_w [T, topk] fp32, or 1 when NULL.
- *  out [T, N] bf16 out; the call zeroes it on the stream, then every slot's
- *  row is added with bf16 atomic adds (each add rounded to bf16).
+ *  out [T, N] bf16 out.  Two accumulations:
+ *   - with a workspace of gg_workspace_size(GG_OP_FORWARD_COMBINE, T, topk,
+ *     E, N, K, 0) bytes (T*N fp32): the call zeroes it, every slot's scaled
+ *     fp32 row is added there with fp32 atomic adds, and one pass rounds the
+ *     sums to bf16 into out (any topk);
+ *   - workspace NULL: out is zeroed and every slot's row, rounded to bf16, is
+ *     added with bf16 atomic adds (each add rounds); topk above
+ *     GG_COMBINE_BF16_MAX_TOPK returns GG_ERR_WORKSPACE, since the summed
+ *     roundings of more slots approach the 1e-2 relative error bound.
  *  NOT deterministic: the order of a token's topk adds depends on scheduling,
  *  so the last bits can differ from run to run; gg_forward with permute_y and
  *  gg_unpermute_combine give the deterministic result (one fp32 sum, rounded
@@ -204,8 +243,8 @@ int gg_forward(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
  *  (the routing-weight gradient of gg_unpermute_combine_bwd) uses that path. */
 int gg_forward_combine(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
                        const int32_t* gather_idx, const float* topk_w, int64_t T, int topk, int E,
-                       int64_t N, int64_t K, int permute_x, gg_bf16* out, int32_t* status,
-                       void* stream);
+                       int64_t N, int64_t K, int permute_x, gg_bf16* out, void* workspace,
+                       size_t workspace_bytes, int32_t* status, void* stream);
 
 /* ------------------------------------------------------ forward + SwiGLU --
  * The forward grouped GEMM with the gated activation fused into its epilogue
@@ -267,10 +306,18 @@ int gg_backward_dX_swiglu(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_
  *     a_i = X[gather_idx[i] / topk] if permute_x else X[i]
  *     g_i = dY[gather_idx[i]]       if permute_y else dY[i]
  *  fp32 accumulate, bf16 out; an expert with no rows gets dW[e] = 0.
- *  X [T, K] if permute_x else [R, K]; dY [R, N]; dW [E, N, K] bf16 out. */
+ *  X [T, K] if permute_x else [R, K]; dY [R, N]; dW [E, N, K] bf16 out.
+ *  workspace (may be NULL): with a permute flag and at least
+ *  gg_workspace_size(GG_OP_BACKWARD_DW, T, topk, E, N, K, flags) bytes, the
+ *  gathered operands are first copied into expert order there (X rows
+ *  R*K*2 bytes, dY rows R*N*2 bytes) and the reduction reads dense tiles;
+ *  with NULL the row gathers are fused into the reduction's operand loads,
+ *  which is several times slower on sm_103a (each reduction block needs 64
+ *  newly gathered rows).  Both give the same products. */
 int gg_backward_dW(const gg_bf16* X, const gg_bf16* dY, const int32_t* m_sizes,
                    const int32_t* gather_idx, int64_t T, int topk, int E, int64_t N, int64_t K,
-                   int permute_x, int permute_y, gg_bf16* dW, int32_t* status, void* stream);
+                   int permute_x, int permute_y, gg_bf16* dW, void* workspace,
+                   size_t workspace_bytes, int32_t* status, void* stream);
 
 /* --------------------------------------------------------- dual asymmetric --
  * Two experts' GEMMs with different row counts and output widths in one
@@ -283,6 +330,41 @@ int gg_backward_dW(const gg_bf16* X, const gg_bf16* dY, const int32_t* m_sizes,
 int gg_dual_asym(const gg_bf16* X0, const gg_bf16* X1, const gg_bf16* W0, const gg_bf16* W1,
                  gg_bf16* Y0, gg_bf16* Y1, int64_t m0, int64_t m1, int64_t k, int64_t n0,
                  int64_t n1, int trans_a, int trans_b, int32_t* status, void* stream);
+
+/* ------------------------------------------------------- expert parallel --
+ * Rows routed to experts held by other ranks ([V] FusedComm and
+ * post_matmul_comm_torch: routed rows exchanged between the ranks that hold
+ * different experts).  G ranks; rank r holds experts [r*E_loc, (r+1)*E_loc),
+ * E = G * E_loc <= GG_MAX_EXPERTS.  After gg_route_hist_offsets and
+ * gg_permute over all E experts, rank r's rows for rank d's experts are the
+ * contiguous block d of its expert-order rows.  The caller exchanges, with
+ * its own collectives (e.g. NCCL all-to-all), first the counts
+ * (recv_m[s][e] = rank s's m_sizes[r*E_loc + e]), then the rows: rank r
+ * receives from each source s, in source order, s's rows for r's experts,
+ * expert after expert.  The local GEMMs want expert-contiguous rows:
+ *   received row j of block (s, e), q-th in it, becomes local row
+ *   row_map[j] = local_off[e] + sum_{s'<s} recv_m[s'][e] + q,
+ * local_off = exclusive prefix of local_m_sizes[e] = sum_s recv_m[s][e]; so
+ * gg_permute(X_recv, row_map, topk = 1) gives them, and after the local
+ * GEMMs gg_unpermute_combine(Y_loc, row_map, NULL, R_loc, 1) puts the results
+ * back in received order for the return exchange.  Within an expert, rows
+ * stay in (source rank, source row) order: the order of one routing of every
+ * rank's tokens numbered rank after rank. */
+
+/* Host-side plan (no GPU work; all arrays host memory).  m_sizes [G*E_loc]:
+ * this rank's histogram over all experts; recv_m [G][E_loc]: received counts.
+ * Out: send_counts [G] rows for each rank, recv_counts [G] rows from each
+ * rank, local_m_sizes [E_loc]; row_map [R_loc] (or NULL) as above, row_map_len
+ * must be R_loc = sum of recv_m.  Negative counts -> GG_ERR_INVALID_ARG. */
+int gg_ep_plan(const int32_t* m_sizes, const int32_t* recv_m, int G, int E_loc, int64_t* send_counts,
+               int64_t* recv_counts, int32_t* local_m_sizes, int32_t* row_map, int64_t row_map_len);
+
+/* The same row_map computed on the device from the device copy of recv_m
+ * [G][E_loc] (int32), for R_loc received rows; row_map [R_loc] int32 out.
+ * R_loc not equal to the sum of recv_m (or a negative count) sets
+ * GG_DEV_SIZES_MISMATCH; rows past the counted ones get -1. */
+int gg_ep_recv_map(const int32_t* recv_m, int G, int E_loc, int64_t R_loc, int32_t* row_map,
+                   int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

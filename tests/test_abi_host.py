@@ -51,19 +51,30 @@ def test_binding_constants_match_header(lib):
 def test_status_strings(lib):
     from unpermute_route_hist_gb300 import _lib
     assert _lib.status_string(0) == "ok"
-    for c in (-1, -2, -3, -6):
+    for c in (-1, -2, -3, -4, -5, -6):
         assert _lib.status_string(c) != "unknown status"
     for c in (1, 2, 3, 4):
         assert _lib.device_status_string(c) != "unknown device status"
 
 
 def test_workspace_size(lib):
-    from unpermute_route_hist_gb300 import api
+    from unpermute_route_hist_gb300 import _lib, api
     assert api.route_workspace_size(0, 1, 4) == 0
     small = api.route_workspace_size(64, 2, 4)
     assert small >= 4 * 4 and small % 256 == 0
     assert api.route_workspace_size(16384, 8, 128) >= 512 * 128 * 4
     assert api.route_workspace_size(-1, 1, 4) == 0
+    ws = api.workspace_size
+    assert ws(_lib.GG_OP_ROUTE, 16384, 8, 128) == api.route_workspace_size(16384, 8, 128)
+    # dW: expert-order copies of the gathered operands, each rounded up to 256 bytes
+    T, k, N, K = 8192, 2, 28672, 4096
+    assert ws(_lib.GG_OP_BACKWARD_DW, T, k, 8, N, K, 0) == 0
+    assert ws(_lib.GG_OP_BACKWARD_DW, T, k, 8, N, K, _lib.GG_PERMUTE_X) == T * k * K * 2
+    assert ws(_lib.GG_OP_BACKWARD_DW, T, k, 8, N, K, _lib.GG_PERMUTE_Y) == T * k * N * 2
+    assert ws(_lib.GG_OP_BACKWARD_DW, 3, 1, 8, 8, 16, 3) == 256 + 256
+    # fused combine: a [T, N] fp32 accumulator
+    assert ws(_lib.GG_OP_FORWARD_COMBINE, 100, 4, 8, 24, 16, 0) == 100 * 24 * 4
+    assert ws(99, 100, 4, 8, 24, 16, 0) == 0 and ws(_lib.GG_OP_ROUTE, -1, 1, 4) == 0
 
 
 def test_host_validation_codes(lib):
@@ -87,7 +98,19 @@ def test_host_validation_codes(lib):
     # dX token sum only with permute_x
     assert L.gg_backward_dX(fake, fake, fake, fake, 4, 2, 4, 8, 8, 0, 1, fake, fake, None, None) == _lib.GG_ERR_INVALID_ARG
     # null outputs
-    assert L.gg_backward_dW(fake, fake, fake, None, 4, 2, 4, 8, 8, 0, 0, None, None, None) == _lib.GG_ERR_INVALID_ARG
+    assert L.gg_backward_dW(fake, fake, fake, None, 4, 2, 4, 8, 8, 0, 0, None, None, 0, None, None) == _lib.GG_ERR_INVALID_ARG
+    # dW with a gathered operand: a workspace too small or misaligned is refused
+    need = L.gg_workspace_size(_lib.GG_OP_BACKWARD_DW, 4, 2, 4, 8, 8, _lib.GG_PERMUTE_X)
+    assert need == 256  # 8 rows x 8 columns x 2 bytes, rounded up to 256
+    assert L.gg_backward_dW(fake, fake, fake, fake, 4, 2, 4, 8, 8, 1, 0, fake, fake, need - 1, None, None) == _lib.GG_ERR_WORKSPACE
+    assert L.gg_backward_dW(fake, fake, fake, fake, 4, 2, 4, 8, 8, 1, 0, fake, odd, need, None, None) == _lib.GG_ERR_WORKSPACE
+    # fused combine: bf16 accumulation (no workspace) refused above its topk limit; a
+    # small fp32 workspace refused
+    assert L.gg_forward_combine(fake, fake, fake, fake, None, 4, _lib.GG_COMBINE_BF16_MAX_TOPK + 1, 4, 8, 8, 0,
+                                fake, None, 0, None, None) == _lib.GG_ERR_WORKSPACE
+    assert L.gg_forward_combine(fake, fake, fake, fake, None, 4, 2, 4, 8, 8, 0, fake, fake, 4 * 8 * 4 - 1,
+                                None, None) == _lib.GG_ERR_WORKSPACE
+    assert L.gg_read_status(None, None, None) == _lib.GG_ERR_INVALID_ARG
     # empty problems are OK without a launch
     assert L.gg_forward(None, None, None, None, None, 0, 2, 4, 8, 8, 0, 0, 0, None, None, None) == _lib.GG_OK
     assert L.gg_permute(None, None, 0, 2, 8, None, None, None) == _lib.GG_OK

@@ -30,6 +30,8 @@ def test_stuck_wait_times_out_with_status(lib):
     assert rc == 0
     assert status_of(st) == _lib.GG_DEV_TIMEOUT
     assert int(result.item()) == 0
+    # gg_read_status maps the device code to the host code for a timeout
+    assert gg.read_status(st) == (_lib.GG_ERR_TIMEOUT, _lib.GG_DEV_TIMEOUT)
     # the context is intact: a grouped GEMM right after is correct
     T, topk, E, K, N = 64, 2, 4, 128, 256
     ids = np.random.default_rng(0).integers(0, E, size=(T, topk)).astype(np.int32)
@@ -39,10 +41,19 @@ def test_stuck_wait_times_out_with_status(lib):
     W = synth.normal_bf16(1, "w", (E, N, K), 0.1)
     st2 = status_tensor()
     Y = gg.forward(dbf(X), dbf(W), r["m_sizes"], r["gather_idx"], None, topk, status=st2)
-    assert status_of(st2) == 0
+    assert gg.read_status(st2) == (_lib.GG_OK, 0)
     assert_close(hbf(Y), orc.forward(X, W, ro["m_sizes"], ro["gather_idx"], None, T, topk, 0, 0, 0),
                  "forward after timeout")
 
 
 def test_selftest_rejects_bad_arguments(lib):
     assert lib.gg_selftest_bounded_wait(None, None, 1000, None) == _lib.GG_ERR_INVALID_ARG
+
+
+def test_read_status_reports_bad_input_data(lib):
+    """An expert id out of range is skipped by the routing kernels and reported
+    through the status word; gg_read_status returns GG_ERR_DEVICE_CHECK."""
+    ids = np.array([[0, 1], [2, 7]], np.int32)  # 7 is outside [0, 4)
+    st = status_tensor()
+    gg.route_hist_offsets(di32(ids), 4, status=st)
+    assert gg.read_status(st) == (_lib.GG_ERR_DEVICE_CHECK, _lib.GG_DEV_BAD_EXPERT_ID)

@@ -73,7 +73,9 @@ def _run_layer(cfg):
     res["dX1"], res["dXt"] = hbf(dX1), hbf(dXt)
     res["dW1"] = hbf(gg.backward_dW(Xp, dH, r["m_sizes"], r["gather_idx"], T, k, status=st))
     res["dW1_fused"] = hbf(gg.backward_dW(X, dH, r["m_sizes"], r["gather_idx"], T, k, True, False,
-                                          status=st))
+                                          workspace=False, status=st))
+    res["dW1_ws"] = hbf(gg.backward_dW(X, dH, r["m_sizes"], r["gather_idx"], T, k, True, False,
+                                       status=st))
     if I:
         A2, W2, G = dbf(host["A2"]), dbf(host["W2"]), dbf(host["G"])
         wt = df32(w)
@@ -90,7 +92,9 @@ def _run_layer(cfg):
                                               status=st))
         res["dW2"] = hbf(gg.backward_dW(A2, dYp, r["m_sizes"], r["gather_idx"], T, k, status=st))
         res["dW2_fused"] = hbf(gg.backward_dW(A2, dY2, r["m_sizes"], r["gather_idx"], T, k, False, True,
-                                              status=st))
+                                              workspace=False, status=st))
+        res["dW2_ws"] = hbf(gg.backward_dW(A2, dY2, r["m_sizes"], r["gather_idx"], T, k, False, True,
+                                           status=st))
     for key in ("m_sizes", "offsets", "padded_offsets", "gather_idx", "row_id_map"):
         res[key] = r[key].cpu().numpy()
     res["status"] = status_of(st)
@@ -133,8 +137,10 @@ def test_full_layer_sampled(name):
     vals = orc.backward_dW_rows(host["X"], host["dH"], m, g, k, 1, 0, es, ns)
     assert_close(res["dW1"][es, ns], vals, name + " dW1")
     assert_close(res["dW1_fused"][es, ns], vals, name + " dW1 (fused token gather)")
+    assert_close(res["dW1_ws"][es, ns], vals, name + " dW1 (token gather into the workspace)")
     for e in empty:
         assert (res["dW1"][e] == 0).all() and (res["dW1_fused"][e] == 0).all()
+        assert (res["dW1_ws"][e] == 0).all()
 
     if I:
         # GEMM2 forward with the scatter to token order (and with the top-k scale)
@@ -172,8 +178,10 @@ def test_full_layer_sampled(name):
         vals = orc.backward_dW_rows(host["A2"], dY2h, m, g, k, 0, 1, es, ns)
         assert_close(res["dW2"][es, ns], vals, name + " dW2")
         assert_close(res["dW2_fused"][es, ns], vals, name + " dW2 (fused slot gather)")
+        assert_close(res["dW2_ws"][es, ns], vals, name + " dW2 (slot gather into the workspace)")
         for e in empty:
             assert (res["dW2"][e] == 0).all() and (res["dW2_fused"][e] == 0).all()
+            assert (res["dW2_ws"][e] == 0).all()
 
 
 def test_mlp8_gemm1_swiglu_sampled():
@@ -205,10 +213,12 @@ def test_mlp8_gemm1_swiglu_sampled():
                  magnitude=np.abs(orc.swiglu_bwd(Href, dA[dest])) * 4)
 
 
-def test_mlp8_gemm2_fused_combine_sampled():
+@pytest.mark.parametrize("fp32", [True, False])
+def test_mlp8_gemm2_fused_combine_sampled(fp32):
     """GEMM2 of mlp8 with the top-k combine fused into the epilogue (the
     inference form), on sampled tokens: each token's slots are computed one by
-    one by the oracle and summed with the routing weights."""
+    one by the oracle and summed with the routing weights.  fp32: sums in the
+    fp32 workspace, one rounding; else bf16 atomic adds into the output."""
     cfg = synth.MLP8
     T, k, E, K, I, R = cfg.T, cfg.topk, cfg.E, cfg.K, cfg.I, cfg.R
     ids, w = synth.route_choices(cfg)
@@ -217,7 +227,7 @@ def test_mlp8_gemm2_fused_combine_sampled():
     dev = torch.device("cuda:0")
     r = gg.route_hist_offsets(torch.from_numpy(ids).to(dev), E, status=st)
     out = gg.forward_combine(dbf(host["A2"]), dbf(host["W2"]), r["m_sizes"], r["gather_idx"], df32(w),
-                             k, False, status=st)
+                             k, False, workspace=None if fp32 else False, status=st)
     outh = hbf(out)
     assert status_of(st) == 0
     ro = orc.route(ids, T, k, E)
@@ -230,7 +240,10 @@ def test_mlp8_gemm2_fused_combine_sampled():
     assert (dest == slots).all()
     ref = vals.reshape(toks.size, k, K).sum(axis=1)
     mag = np.abs(vals).reshape(toks.size, k, K).sum(axis=1)
-    assert_close(outh[toks], ref, "mlp8 GEMM2 fused combine", magnitude=(k + 1) / 4.0 * mag)
+    if fp32:
+        assert_close(outh[toks], ref, "mlp8 GEMM2 fused combine (fp32 sums)")
+    else:
+        assert_close(outh[toks], ref, "mlp8 GEMM2 fused combine (bf16 adds)", magnitude=(k + 1) / 4.0 * mag)
 
 
 def test_mlp8_dX2_swiglu_sampled():

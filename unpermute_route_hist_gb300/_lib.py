@@ -23,6 +23,8 @@ SIGNATURES = {
     "gg_status_string": (_cstr, [_int]),
     "gg_device_status_string": (_cstr, [_int]),
     "gg_last_cuda_error": (_cstr, []),
+    "gg_workspace_size": (_sz, [_int, _i64, _int, _int, _i64, _i64, _int]),
+    "gg_read_status": (_int, [_vp, _vp, _vp]),
     "gg_selftest_bounded_wait": (_int, [_vp, _vp, ctypes.c_uint64, _vp]),
     "gg_route_workspace_size": (_sz, [_i64, _int, _int]),
     "gg_route_hist_offsets": (_int, [_vp, _i64, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -35,7 +37,7 @@ SIGNATURES = {
     "gg_forward": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _int, _int,
                           _vp, _vp, _vp]),
     "gg_forward_combine": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _vp,
-                                  _vp, _vp]),
+                                  _vp, _sz, _vp, _vp]),
     "gg_forward_swiglu": (_int, [_vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _vp, _vp,
                                  _vp, _vp]),
     "gg_swiglu_bwd": (_int, [_vp, _vp, _i64, _i64, _vp, _vp]),
@@ -44,15 +46,19 @@ SIGNATURES = {
     "gg_backward_dX_swiglu": (_int, [_vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _vp, _vp, _vp,
                                      _vp]),
     "gg_backward_dW": (_int, [_vp, _vp, _vp, _vp, _i64, _int, _int, _i64, _i64, _int, _int, _vp, _vp,
-                              _vp]),
+                              _sz, _vp, _vp]),
     "gg_dual_asym": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _int, _int,
                             _vp, _vp]),
+    "gg_ep_plan": (_int, [_vp, _vp, _int, _int, _vp, _vp, _vp, _vp, _i64]),
+    "gg_ep_recv_map": (_int, [_vp, _int, _int, _i64, _vp, _vp, _vp]),
 }
 
 GG_OK = 0
 GG_ERR_INVALID_ARG = -1
 GG_ERR_UNSUPPORTED = -2
 GG_ERR_CUDA = -3
+GG_ERR_DEVICE_CHECK = -4
+GG_ERR_TIMEOUT = -5
 GG_ERR_WORKSPACE = -6
 GG_DEV_OK = 0
 GG_DEV_BAD_EXPERT_ID = 1
@@ -62,6 +68,12 @@ GG_DEV_TIMEOUT = 4
 GG_MAX_EXPERTS = 2048
 GG_MAX_TOPK = 64
 GG_ROUTE_NOALLOC_SCRATCH_BYTES = 1 << 20
+GG_COMBINE_BF16_MAX_TOPK = 16
+GG_OP_ROUTE = 1
+GG_OP_BACKWARD_DW = 2
+GG_OP_FORWARD_COMBINE = 3
+GG_PERMUTE_X = 1
+GG_PERMUTE_Y = 2
 
 _lock = threading.Lock()
 _lib = None

@@ -50,6 +50,38 @@ def route_workspace_size(T: int, topk: int, E: int) -> int:
     return int(_lib.load().gg_route_workspace_size(T, topk, E))
 
 
+def workspace_size(op: int, T: int, topk: int, E: int, N: int = 0, K: int = 0, flags: int = 0) -> int:
+    """Bytes of workspace for gg_* entry point `op` (_lib.GG_OP_*) on this problem."""
+    return int(_lib.load().gg_workspace_size(op, T, topk, E, N, K, flags))
+
+
+def read_status(status):
+    """(rc, code): synchronise the current stream, read the device status word;
+    rc is GG_OK, GG_ERR_DEVICE_CHECK or GG_ERR_TIMEOUT, code the GG_DEV_* value."""
+    import ctypes
+    _need(status, torch.int32, "status", (1,))
+    code = ctypes.c_int32(0)
+    rc = _lib.load().gg_read_status(_p(status), ctypes.addressof(code), _stream(status.device))
+    if rc == _lib.GG_ERR_CUDA:
+        _lib.check("gg_read_status", rc)
+    return rc, int(code.value)
+
+
+def _workspace(ws, nbytes, device):
+    """A caller's workspace tensor, False (none), or None: allocate one of nbytes."""
+    if ws is False or nbytes == 0:
+        return None
+    if ws is None:
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return ws
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
 def route_hist_offsets(topk_ids, E: int, pad_block: int = 0, *, workspace=None, status=None,
                        row_id_map: bool = True, outs: dict | None = None) -> dict:
     """m_sizes, offsets, padded_offsets (pad_block > 0), gather_idx, row_id_map."""
@@ -143,9 +175,11 @@ def forward(X, W, m_sizes, gather_idx, topk_w, topk: int, permute_x=False, permu
 
 
 def forward_combine(X, W, m_sizes, gather_idx, topk_w, topk: int, permute_x=False, *, out=None,
-                    status=None):
+                    workspace=None, status=None):
     """out [T, N]: forward with the weighted top-k combine fused (atomic adds,
-    not bit-deterministic); topk_w [T, topk] fp32 or None (unit weights)."""
+    not bit-deterministic); topk_w [T, topk] fp32 or None (unit weights).
+    workspace: None allocates the T*N fp32 accumulator, a tensor is used as it,
+    False selects bf16 accumulation in out (topk <= GG_COMBINE_BF16_MAX_TOPK)."""
     _need(X, torch.bfloat16, "X")
     _need(W, torch.bfloat16, "W")
     E, N, K = W.shape
@@ -160,8 +194,10 @@ def forward_combine(X, W, m_sizes, gather_idx, topk_w, topk: int, permute_x=Fals
     if topk_w is not None and topk_w.numel() != R:
         raise ValueError("topk_w must have T*topk elements")
     out = _out(out, (T, N), torch.bfloat16, X.device, "out")
+    ws = _workspace(workspace, workspace_size(_lib.GG_OP_FORWARD_COMBINE, T, topk, E, N, K), X.device)
     rc = _lib.load().gg_forward_combine(_p(X), _p(W), _p(m_sizes), _p(gather_idx), _p(topk_w), T, topk,
-                                        E, N, K, int(permute_x), _p(out), _p(status), _stream(X.device))
+                                        E, N, K, int(permute_x), _p(out), _p(ws), _nbytes(ws),
+                                        _p(status), _stream(X.device))
     _lib.check("gg_forward_combine", rc)
     return out
 
@@ -235,7 +271,10 @@ def backward_dX_swiglu(dY, W, m_sizes, topk: int, H, *, out=None, status=None):
 
 
 def backward_dW(X, dY, m_sizes, gather_idx, T: int, topk: int, permute_x=False, permute_y=False,
-                *, out=None, status=None):
+                *, out=None, workspace=None, status=None):
+    """dW [E, N, K].  With a permute flag, workspace None allocates the buffer
+    for the expert-order copies of the gathered operands (the fast path), a
+    tensor is used as it, False fuses the row gathers into the operand loads."""
     _need(X, torch.bfloat16, "X")
     _need(dY, torch.bfloat16, "dY")
     E = m_sizes.shape[0]
@@ -247,9 +286,11 @@ def backward_dW(X, dY, m_sizes, gather_idx, T: int, topk: int, permute_x=False, 
         raise ValueError("X must have T (permute_x) or T*topk rows; dY T*topk rows")
     _opt(gather_idx, torch.int32, "gather_idx", (R,))
     dW = _out(out, (E, N, K), torch.bfloat16, X.device, "out")
+    flags = (_lib.GG_PERMUTE_X if permute_x else 0) | (_lib.GG_PERMUTE_Y if permute_y else 0)
+    ws = _workspace(workspace, workspace_size(_lib.GG_OP_BACKWARD_DW, T, topk, E, N, K, flags), X.device)
     rc = _lib.load().gg_backward_dW(_p(X), _p(dY), _p(m_sizes), _p(gather_idx), T, topk, E, N, K,
-                                    int(permute_x), int(permute_y), _p(dW), _p(status),
-                                    _stream(X.device))
+                                    int(permute_x), int(permute_y), _p(dW), _p(ws), _nbytes(ws),
+                                    _p(status), _stream(X.device))
     _lib.check("gg_backward_dW", rc)
     return dW
 

@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libgg.so")
 
-SOURCES = ["abi.cu", "route.cu", "route_noalloc.cu", "move.cu", "gemm_ragged_m.cu", "gemm_dw.cu", "gemm_dual.cu"]
+SOURCES = ["abi.cu", "route.cu", "route_noalloc.cu", "move.cu", "gemm_ragged_m.cu", "gemm_dw.cu", "gemm_dual.cu", "ep.cu"]
 HEADERS = ["common.cuh", "gemm_engine.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -25,6 +25,7 @@ int swiglu_bwd_launch(const uint16_t* H, const uint16_t* dA, int64_t rows, int64
 int combine_bwd_launch(const uint16_t* G, const uint16_t* Y, const int32_t* row_id_map,
                        const float* topk_w, int64_t T, int topk, int64_t N, uint16_t* dY, float* dw,
                        int32_t* status, cudaStream_t stream);
+size_t backward_dw_workspace_bytes(int64_t T, int topk, int64_t N, int64_t K, int flags);
 
 namespace {
 thread_local char g_last_error[256] = "no error";
@@ -161,7 +162,9 @@ const char* gg_status_string(int code) {
         case GG_ERR_INVALID_ARG: return "invalid argument";
         case GG_ERR_UNSUPPORTED: return "unsupported shape, alignment or size";
         case GG_ERR_CUDA: return "CUDA error (see gg_last_cuda_error)";
-        case GG_ERR_WORKSPACE: return "workspace too small";
+        case GG_ERR_DEVICE_CHECK: return "a kernel found bad input data (see the device status code)";
+        case GG_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+        case GG_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         default: return "unknown status";
     }
 }
@@ -182,6 +185,28 @@ const char* gg_last_cuda_error(void) { return g_last_error; }
 size_t gg_route_workspace_size(int64_t T, int topk, int E) {
     if (T < 0 || topk < 1 || E < 1) return 0;
     return route_workspace_bytes(T, topk, E);
+}
+
+size_t gg_workspace_size(int op, int64_t T, int topk, int E, int64_t N, int64_t K, int flags) {
+    if (T < 0 || topk < 1 || E < 1 || N < 0 || K < 0) return 0;
+    switch (op) {
+        case GG_OP_ROUTE: return route_workspace_bytes(T, topk, E);
+        case GG_OP_BACKWARD_DW: return backward_dw_workspace_bytes(T, topk, N, K, flags);
+        case GG_OP_FORWARD_COMBINE: return static_cast<size_t>(T) * static_cast<size_t>(N) * sizeof(float);
+        default: return 0;
+    }
+}
+
+int gg_read_status(const int32_t* status, int32_t* code, void* stream) {
+    if (!status) return GG_ERR_INVALID_ARG;
+    int32_t v = 0;
+    // a copy into this stack word: the runtime stages it, nothing is allocated here
+    cudaError_t e = cudaMemcpyAsync(&v, status, sizeof v, cudaMemcpyDeviceToHost, as_stream(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+    if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+    if (code) *code = v;
+    if (v == GG_DEV_OK) return GG_OK;
+    return v == GG_DEV_TIMEOUT ? GG_ERR_TIMEOUT : GG_ERR_DEVICE_CHECK;
 }
 
 int gg_route_hist_offsets(const int32_t* topk_ids, int64_t T, int topk, int E, int pad_block,

@@ -416,6 +416,13 @@ __device__ __forceinline__ void red_add_bf16x8(void* ptr, const uint4& v) {
                  : "memory");
 }
 
+// Four fp32 atomic adds to consecutive floats (16-byte aligned), one vector op.
+__device__ __forceinline__ void red_add_f32x4(float* ptr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }

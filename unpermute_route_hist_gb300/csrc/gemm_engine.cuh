@@ -89,6 +89,9 @@ struct GemmParams {
     // RAGGED_M: add row i (scaled) into token row gather_idx[i] / topk of a
     // zeroed [T, N] output with bf16 atomic adds (the top-k combine, fused)
     int combine_out;
+    // RAGGED_M with combine_out: add the scaled fp32 rows into this zeroed
+    // [T, N] fp32 buffer with fp32 atomic adds instead (out is then null)
+    float* acc_out;
     // RAGGED_M: the output is the upstream gradient dA of a SwiGLU over
     // interleaved gate/up columns; instead of dA, store dH[i, 2c], dH[i, 2c+1]
     // into out (ld_out = 2N) from the stored pre-activation H[i, 2c], H[i, 2c+1]
@@ -769,6 +772,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 }
             }
             uint16_t* orow = (dest >= 0 && out) ? out + dest * ld : nullptr;
+            float* frow = (KIND == KIND_RAGGED_M && dest >= 0 && p.acc_out) ? p.acc_out + dest * ld : nullptr;
             uint16_t* arow_out = (KIND == KIND_RAGGED_M && dest >= 0 && p.act_out) ? p.act_out + dest * p.ld_act : nullptr;
             if (ti.nkb == 0) {
                 if (orow) {
@@ -838,6 +842,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             // convert and store 32 accumulator columns starting at output column col0,
             // straight from registers (16 bytes of the thread's own row per store)
             auto store_out32 = [&](const uint32_t (&v)[32], int col0) {
+                if (KIND == KIND_RAGGED_M && frow) {
+#pragma unroll
+                    for (int pc = 0; pc < 8; ++pc) {
+                        const int col = col0 + pc * 4;
+                        if (col < ncols)
+                            red_add_f32x4(frow + col, __uint_as_float(v[pc * 4 + 0]) * sc,
+                                          __uint_as_float(v[pc * 4 + 1]) * sc,
+                                          __uint_as_float(v[pc * 4 + 2]) * sc,
+                                          __uint_as_float(v[pc * 4 + 3]) * sc);
+                    }
+                }
                 if (orow) {
 #pragma unroll
                     for (int pc = 0; pc < 4; ++pc) {

@@ -1,7 +1,7 @@
 // gemm_ragged_m.cu -- entry points whose output rows are ragged per expert:
 // the forward grouped GEMM (also with the fused SwiGLU of matmul_ogs.py's
 // FusedActivation, or with the top-k combine fused into the epilogue as
-// atomic adds) and the backward dX (interface.py, grouped_gemm_forward
+// fp32 or bf16 atomic adds) and the backward dX (interface.py, grouped_gemm_forward
 // and grouped_gemm_dX), also with the SwiGLU backward fused into its epilogue.  Both run the persistent tcgen05
 // engine of gemm_engine.cuh over the expert-order row tiles.
 #include "gemm_engine.cuh"
@@ -9,6 +9,7 @@
 namespace gg {
 int combine_launch(const uint16_t* Y, const int32_t* row_id_map, const float* topk_w, int64_t T,
                    int topk, int64_t N, uint16_t* out, int32_t* status, cudaStream_t stream);
+int f32_to_bf16_launch(const float* src, int64_t n, uint16_t* dst, cudaStream_t stream);
 }
 
 using namespace gg;
@@ -123,8 +124,8 @@ int gg_forward_swiglu(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes
 
 int gg_forward_combine(const gg_bf16* X, const gg_bf16* W, const int32_t* m_sizes,
                        const int32_t* gather_idx, const float* topk_w, int64_t T, int topk, int E,
-                       int64_t N, int64_t K, int permute_x, gg_bf16* out, int32_t* status,
-                       void* stream) {
+                       int64_t N, int64_t K, int permute_x, gg_bf16* out, void* workspace,
+                       size_t workspace_bytes, int32_t* status, void* stream) {
     if (T < 0 || topk < 1 || E < 1 || N < 0 || K < 0) return GG_ERR_INVALID_ARG;
     if (topk > GG_MAX_TOPK || E > GG_MAX_EXPERTS || N % 8 || K % 8) return GG_ERR_UNSUPPORTED;
     const int64_t R = T * topk;
@@ -135,28 +136,40 @@ int gg_forward_combine(const gg_bf16* X, const gg_bf16* W, const int32_t* m_size
     if (!al16(out)) return GG_ERR_UNSUPPORTED;
     if (K > 0 && (!X || !W)) return GG_ERR_INVALID_ARG;  // with K == 0 they have no elements
     if (K > 0 && (!al16(X) || !al16(W))) return GG_ERR_UNSUPPORTED;
+    // fp32 sums in the caller's workspace, or (small topk only) bf16 adds into out
+    const size_t acc_bytes = static_cast<size_t>(T) * static_cast<size_t>(N) * sizeof(float);
+    const bool fp32 = workspace != nullptr;
+    if (fp32 && (workspace_bytes < acc_bytes || !al16(workspace))) return GG_ERR_WORKSPACE;
+    if (!fp32 && topk > GG_COMBINE_BF16_MAX_TOPK) return GG_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // the adds accumulate into a zeroed output (every token row gets topk adds)
-    cudaError_t e = cudaMemsetAsync(out, 0, static_cast<size_t>(T * N) * 2, st);
-    if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
-    if (K == 0) return GG_OK;
-    GemmParams p = base_params(E, topk, R, m_sizes, gather_idx, status);
-    p.N = static_cast<int>(N);
-    p.Kred = static_cast<int>(K);
-    p.out = out;
-    p.ld_out = N;
-    p.combine_out = 1;
-    p.scale = topk_w;
-    CUtensorMap mA{}, mB{};
-    const int64_t bound = row_tile_bound(R, E) * ((N + kBN - 1) / kBN);
-    if (permute_x) {
-        if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN)) return GG_ERR_CUDA;
-        p.ga = GatherSrc{X, K, T, K, ROW_TOKEN};
-        return launch_gemm<KIND_RAGGED_M, false, false, true, false, false>(mB, mB, mB, mB, p, bound, st);
+    float* acc = static_cast<float*>(workspace);
+    // the adds accumulate into zeroed sums (every token row gets topk adds)
+    int rc = fp32 ? cuda_result(cudaMemsetAsync(acc, 0, acc_bytes, st))
+                  : cuda_result(cudaMemsetAsync(out, 0, static_cast<size_t>(T * N) * 2, st));
+    if (rc != GG_OK) return rc;
+    if (K > 0) {
+        GemmParams p = base_params(E, topk, R, m_sizes, gather_idx, status);
+        p.N = static_cast<int>(N);
+        p.Kred = static_cast<int>(K);
+        p.out = fp32 ? nullptr : out;
+        p.acc_out = fp32 ? acc : nullptr;
+        p.ld_out = N;
+        p.combine_out = 1;
+        p.scale = topk_w;
+        CUtensorMap mA{}, mB{};
+        const int64_t bound = row_tile_bound(R, E) * ((N + kBN - 1) / kBN);
+        if (permute_x) {
+            if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN)) return GG_ERR_CUDA;
+            p.ga = GatherSrc{X, K, T, K, ROW_TOKEN};
+            rc = launch_gemm<KIND_RAGGED_M, false, false, true, false, false>(mB, mB, mB, mB, p, bound, st);
+        } else {
+            if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN / 2)) return GG_ERR_CUDA;
+            if (!encode_map_2d(&mA, X, K, R, K, kBK, kBM)) return GG_ERR_CUDA;
+            rc = launch_gemm<KIND_RAGGED_M, false, false, false, false, true>(mA, mB, mA, mB, p, bound, st);
+        }
+        if (rc != GG_OK) return rc;
     }
-    if (!encode_map_3d(&mB, W, K, N, E, K, N * K, kBK, kBN / 2)) return GG_ERR_CUDA;
-    if (!encode_map_2d(&mA, X, K, R, K, kBK, kBM)) return GG_ERR_CUDA;
-    return launch_gemm<KIND_RAGGED_M, false, false, false, false, true>(mA, mB, mA, mB, p, bound, st);
+    return fp32 ? f32_to_bf16_launch(acc, T * N, out, st) : GG_OK;
 }
 
 int gg_backward_dX(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_sizes,

@@ -13,6 +13,10 @@
 //  combine backward   its gradient (backend.py, unpermute_bwd): each slot's row
 //                     gets the token's output gradient times the slot weight,
 //                     and each weight gets <output gradient, forward row>.
+//  gather rows        expert-order copies of gathered operands for dW
+//                     (interface.py, grouped_gemm_dW with permute_x/permute_y),
+//                     so its reduction reads dense tiles.
+//  fp32 -> bf16       the final rounding of the fused combine's fp32 sums.
 //
 // They move whole rows as 16-byte vectors (row widths are multiples of 8
 // bf16): permute and combine one warp per token row, the combine backward one
@@ -258,6 +262,52 @@ swiglu_bwd_kernel(const uint4* __restrict__ H, const uint4* __restrict__ dA, int
     }
 }
 
+// Row gather into expert order: dst[i] = src[gather_idx[i] / div] for every
+// expert-order row i (div = topk: token rows; 1: token-slot rows).  One warp
+// per destination row, kVecsInFlight 16-byte loads in flight per lane.  An
+// index outside the source sets GG_DEV_BAD_ROW_INDEX and the row is zeroed.
+__global__ void __launch_bounds__(kMoveThreads)
+gather_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ gather_idx, int div,
+                   int64_t src_rows, int64_t R, int64_t row_vecs, uint4* __restrict__ dst,
+                   int32_t* status) {
+    const int lane = lane_id();
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarpsPerCta;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + warp_id(); i < R; i += nwarps) {
+        const int32_t f = gather_idx[i];
+        int64_t r = f < 0 ? -1 : static_cast<int64_t>(static_cast<uint32_t>(f) / static_cast<uint32_t>(div));
+        if (r < 0 || r >= src_rows) {
+            if (lane == 0) set_status(status, GG_DEV_BAD_ROW_INDEX);
+            r = -1;
+        }
+        const uint4* s = src + r * row_vecs;
+        uint4* d = dst + i * row_vecs;
+        for (int64_t c0 = 0; c0 < row_vecs; c0 += 32 * kVecsInFlight) {
+            uint4 v[kVecsInFlight];
+#pragma unroll
+            for (int u = 0; u < kVecsInFlight; ++u) {
+                const int64_t c = c0 + u * 32 + lane;
+                v[u] = (c < row_vecs && r >= 0) ? ld_stream(s + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kVecsInFlight; ++u) {
+                const int64_t c = c0 + u * 32 + lane;
+                if (c < row_vecs) d[c] = v[u];
+            }
+        }
+    }
+}
+
+// fp32 -> bf16 (round to nearest even), 8 values per thread and step.
+__global__ void __launch_bounds__(kMoveThreads)
+f32_to_bf16_kernel(const float4* __restrict__ src, int64_t groups, uint4* __restrict__ dst) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x; i < groups;
+         i += static_cast<int64_t>(gridDim.x) * kMoveThreads) {
+        const float4 a = src[2 * i], b = src[2 * i + 1];
+        dst[i] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                            pack_bf16x2(b.z, b.w));
+    }
+}
+
 unsigned move_grid(int64_t rows) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -299,6 +349,27 @@ int combine_bwd_launch(const uint16_t* G, const uint16_t* Y, const int32_t* row_
     combine_bwd_kernel<<<move_grid(T), kMoveThreads, 0, stream>>>(
         reinterpret_cast<const uint4*>(G), reinterpret_cast<const uint4*>(Y), row_id_map, topk_w, T,
         topk, N / 8, R, reinterpret_cast<uint4*>(dY), dw, status);
+    return launch_result();
+}
+
+int gather_rows_launch(const uint16_t* src, const int32_t* gather_idx, int div, int64_t src_rows,
+                       int64_t R, int64_t cols, uint16_t* dst, int32_t* status, cudaStream_t stream) {
+    clear_pending_launch_error();
+    gather_rows_kernel<<<move_grid((R + kWarpsPerCta - 1) / kWarpsPerCta), kMoveThreads, 0, stream>>>(
+        reinterpret_cast<const uint4*>(src), gather_idx, div, src_rows, R, cols / 8,
+        reinterpret_cast<uint4*>(dst), status);
+    return launch_result();
+}
+
+int f32_to_bf16_launch(const float* src, int64_t n, uint16_t* dst, cudaStream_t stream) {
+    const int64_t groups = n / 8;
+    int64_t blocks = (groups + kMoveThreads - 1) / kMoveThreads;
+    const int64_t cap = static_cast<int64_t>(move_grid(INT64_MAX)) * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) return GG_OK;
+    clear_pending_launch_error();
+    f32_to_bf16_kernel<<<static_cast<unsigned>(blocks), kMoveThreads, 0, stream>>>(
+        reinterpret_cast<const float4*>(src), groups, reinterpret_cast<uint4*>(dst));
     return launch_result();
 }
 
