@@ -688,6 +688,31 @@ def run_only(args, cfg):
         return (torch.randn(*shape, device=dev, generator=gen) * 0.02).to(bf)
 
     name = args.only
+    if name == "dual":
+        # the two-expert GEMM at its stated shape, L2 flushed before each call
+        d = synth.DUAL
+        X0, X1 = rnd(d.m0, d.k) * 50, rnd(d.m1, d.k) * 50
+        W0, W1 = rnd(d.k, d.n0) * 50, rnd(d.k, d.n1) * 50
+        Y0 = torch.empty(d.m0, d.n0, dtype=bf, device=dev)
+        Y1 = torch.empty(d.m1, d.n1, dtype=bf, device=dev)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush = torch.empty(2 * l2 // 4, dtype=torch.int32, device=dev)
+        for _ in range(max(args.warmup, 1)):
+            gg.dual_asym(X0, X1, W0, W1, out0=Y0, out1=Y1)
+        times = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            gg.dual_asym(X0, X1, W0, W1, out0=Y0, out1=Y1)
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        fl = 2.0 * d.k * (d.m0 * d.n0 + d.m1 * d.n1)
+        ms = statistics.median(times)
+        print(json.dumps({"pass": "dual", "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                          "note": "diagnostic, not a bench line; L2 flushed before each call"}), flush=True)
+        return
     if name == "fwd1":
         Xp, W1 = rnd(R, K), rnd(E, N1, K)
         H, A2 = torch.empty(R, N1, dtype=bf, device=dev), torch.empty(R, I, dtype=bf, device=dev)
@@ -812,18 +837,34 @@ def measure_suite(dev, tflops_sus, hbm_gbs, src_kind):
         ms = timed(lambda: gg.permute(X, rim, k, out=Xp))
         res["permute"] = {"ms": ms, "GBps": perm_b / (ms * 1e-3) / 1e9,
                           "frac_of_hbm": perm_b / (ms * 1e-3) / 1e9 / hbm_gbs}
-        # bytes: GEMM operands and output (bf16); dX1 adds its top-k token sum (R rows
-        # read, T rows written)
+        # bytes: GEMM operands and output (bf16)
         g1 = 2.0 * (R * K + E * N1 * K + R * N1)
+        dX1 = torch.empty(R, K, dtype=bf, device=dev)
+        dXt = torch.empty(T, K, dtype=bf, device=dev)
         passes = {
             "fwd1": (lambda: gg.forward(Xp, W1, m, gi, None, k, False, False, False, out=H), 2.0 * R * N1 * K, g1),
-            "dX1": (lambda: gg.backward_dX(dH, W1, m, gi, T, k, True, False, token_sum=True), 2.0 * R * N1 * K,
-                    g1 + 2.0 * (R * K + T * K)),
+            # dX1 GEMM with the scatter store to token-slot order
+            "dX1": (lambda: gg.backward_dX(dH, W1, m, gi, T, k, True, False, out=dX1), 2.0 * R * N1 * K,
+                    2.0 * (R * N1 + E * N1 * K + R * K)),
             "dW1": (lambda: gg.backward_dW(Xp, dH, m, gi, T, k, False, False), 2.0 * R * N1 * K, g1),
         }
         for name, (fn, fl, nb) in passes.items():
             res[name] = entry(timed(fn), fl, nb)
-        del Xp, W1, dH, H
+        # dX1's top-k token sum, an HBM-bound pass after the GEMM (R rows read, T
+        # written), and the pair as the benchmark step runs it, against the serial
+        # roofline of the two: flops / peak + token-sum bytes / HBM
+        sum_b = 2.0 * (R * K + T * K)
+        ms = timed(lambda: gg.unpermute_combine(dX1, None, None, T, k, out=dXt))
+        res["dX1_token_sum"] = {"ms": ms, "GBps": sum_b / (ms * 1e-3) / 1e9,
+                                "frac_of_hbm": sum_b / (ms * 1e-3) / 1e9 / hbm_gbs}
+        fl1 = 2.0 * R * N1 * K
+        ms = timed(lambda: gg.backward_dX(dH, W1, m, gi, T, k, True, False, token_sum=True, out=dX1,
+                                          out_tok=dXt))
+        serial_ms = fl1 / (tflops_sus * 1e12) * 1e3 + sum_b / (hbm_gbs * 1e9) * 1e3
+        res["dX1_with_token_sum"] = {"ms": ms, "tflops": fl1 / (ms * 1e-3) / 1e12,
+                                     "serial_cap_tflops": fl1 / (serial_ms * 1e-3) / 1e12,
+                                     "frac_of_serial_cap": serial_ms / ms}
+        del Xp, W1, dH, H, dX1, dXt
         if I:
             A2, W2, dYp = rnd(R, I), rnd(E, K, I), rnd(R, K)
             Y2 = torch.empty(R, K, dtype=bf, device=dev)
@@ -838,7 +879,7 @@ def measure_suite(dev, tflops_sus, hbm_gbs, src_kind):
             res["combine"] = {"ms": ms, "GBps": comb_b / (ms * 1e-3) / 1e9,
                               "frac_of_hbm": comb_b / (ms * 1e-3) / 1e9 / hbm_gbs}
             del A2, W2, dYp, Y2
-        gemm = [n for n in res if "tflops" in res[n]]
+        gemm = [n for n in res if "cap_tflops" in res[n]]
         tot_ms = sum(res[n]["ms"] for n in gemm)
         tot_fl = 3.0 * (2.0 * R * N1 * K + (2.0 * R * K * I if I else 0.0))
         out[cfg.name] = {
@@ -907,7 +948,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-suite", action="store_true",
                     help="leave fine128, zipf64 and the dual GEMM out of the bench line")
-    ap.add_argument("--only", choices=["fwd1", "fwd2", "dX2", "dW2", "dX1", "dW1"],
+    ap.add_argument("--only", choices=["fwd1", "fwd2", "dX2", "dW2", "dX1", "dW1", "dual"],
                     help="time one GEMM pass alone on its own operands (for profiling)")
     ap.add_argument("--suite", action="store_true",
                     help="time only fine128, zipf64 and the dual GEMM (a diagnostic line, not the bench line)")

@@ -29,7 +29,7 @@ def _worker(rank, world, port, out):
 
 def test_two_rank_aggregation_takes_the_slowest_rank():
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
