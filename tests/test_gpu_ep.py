@@ -182,3 +182,44 @@ def test_recv_map_kernel_matches_host_plan(G, E_loc):
     rmap2 = ep.recv_map(di32(recv), G, E_loc, int(recv.sum()) + 3, status=st2)
     assert status_of(st2) == gg._lib.GG_DEV_SIZES_MISMATCH
     assert (rmap2.cpu().numpy()[-3:] == -1).all()
+
+
+def test_expert_parallel_through_nccl_one_rank():
+    """The default exchange (torch.distributed all-to-all over NCCL) on a
+    one-rank group: the whole dispatch / combine / backward chain with real
+    collectives (each exchange a copy to itself), against the oracle."""
+    import socket
+
+    import torch.distributed as dist
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % port, rank=0, world_size=1,
+                            device_id=torch.device("cuda:0"))
+    try:
+        c = dict(G=1, T=[150], topk=2, E=4, K=64, N=128, seed=5)
+        ids, w, X, W, Gr = _data(c)
+        T, k, K, N, E = 150, 2, 64, 128, 4
+        epr = ep.ExpertParallel(E, 0, 1)  # TorchDistExchange on the default group
+        st = status_tensor()
+        d = epr.dispatch(dbf(X), di32(ids), status=st)
+        y = gg.forward(d.x, dbf(W), d.m_sizes, None, None, 1, status=st)
+        out = epr.combine(y, d, df32(w), status=st)
+        dy, dw = epr.combine_backward(dbf(Gr), d, df32(w), status=st)
+        dX = epr.dispatch_backward(gg.backward_dX(dy, dbf(W), d.m_sizes, None, d.x.shape[0], 1, status=st), d,
+                                   status=st)
+        assert status_of(st) == 0
+        rg = orc.route(ids, T, k, E)
+        np.testing.assert_array_equal(hbf(d.x), orc.permute(X, rg["gather_idx"], k))
+        Yh = orc.round_bf16(orc.forward(X, W, rg["m_sizes"], rg["gather_idx"], None, T, k, 1, 1, 0))
+        mag = (np.abs(orc.widen_bf16(Yh)).reshape(T, k, N) * w[:, :, None]).sum(axis=1)
+        assert_close(hbf(out), orc.unpermute_combine(Yh, None, w, T, k), "EP over NCCL out", magnitude=mag)
+        dY2, dw_ref = orc.unpermute_combine_bwd(Gr, Yh, None, w, T, k)
+        dXh = orc.round_bf16(orc.backward_dX(orc.round_bf16(dY2), W, rg["m_sizes"], rg["gather_idx"], T, k, 1, 1))
+        assert_close(hbf(dX), orc.topk_sum(dXh, T, k), "EP over NCCL dX",
+                     magnitude=np.abs(orc.widen_bf16(dXh)).reshape(T, k, K).sum(axis=1))
+        bound = 2.0 ** -7 * np.einsum("tn,tjn->tj", np.abs(orc.widen_bf16(Gr)),
+                                      np.abs(orc.widen_bf16(Yh)).reshape(T, k, N)) + 1e-6
+        assert (np.abs(dw.cpu().numpy() - dw_ref) <= bound).all()
+    finally:
+        dist.destroy_process_group()
