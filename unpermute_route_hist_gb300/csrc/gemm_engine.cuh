@@ -119,6 +119,16 @@ struct TileInfo {
     int nkb;        // reduction blocks
 };
 
+// RAGGED_K: experts are scheduled longest first, bucketed by their reduction
+// block count in quarter octaves (bucket 0: no rows)
+constexpr int kOrdBuckets = 128;
+__device__ __forceinline__ int expert_size_bucket(int nblocks) {
+    if (nblocks <= 0) return 0;
+    const int lg = 31 - __clz(nblocks);
+    const int frac = lg >= 2 ? ((nblocks >> (lg - 2)) & 3) : (lg == 1 ? ((nblocks & 1) << 1) : 0);
+    return min(kOrdBuckets - 1, 1 + 4 * lg + frac);
+}
+
 struct SharedCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
@@ -132,6 +142,7 @@ struct SharedCtl {
     int abort_flag;
     int bad_sizes;
     int64_t total_tiles;
+    int32_t ord_start[kOrdBuckets];  // RAGGED_K: expert-order counting sort (prologue only)
 };
 
 // Tiles are scheduled in "units": one m-tile, or (PAIR) two adjacent m-tiles
@@ -182,8 +193,11 @@ __device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
         const int ut_per = (mt_per + U - 1) / U;
         const int nt_per = (p.N + kBN - 1) / kBN;
         const int64_t per_e = static_cast<int64_t>(ut_per) * nt_per;
-        const int e = static_cast<int>(t / per_e);
-        const int loc = static_cast<int>(t - e * per_e);
+        // tiles come expert after expert in s_tp's order (longest reduction first,
+        // written by the prologue in place of RAGGED_M's tile prefix)
+        const int pos = static_cast<int>(t / per_e);
+        const int e = s_tp[pos];
+        const int loc = static_cast<int>(t - static_cast<int64_t>(pos) * per_e);
         // grouped raster inside the expert: kGroupU units x every n-tile, m
         // fastest, so concurrent CTAs share both A and B tiles in L2 and no
         // single tile is read by every SM at once
@@ -415,6 +429,55 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             } else {
                 total_tiles = static_cast<int64_t>(p.E) * (((p.M + kBM - 1) / kBM + (PAIR ? 1 : 0)) / (PAIR ? 2 : 1)) *
                               ((p.N + kBN - 1) / kBN);
+            }
+            if (KIND == KIND_RAGGED_K) {
+                // Longest-first expert order into s_tp: a stable counting sort by size
+                // bucket, descending.  Chunks of 32 experts are visited in order and
+                // ranked within a chunk by lane, so every CTA computes the same order.
+                // A dW tile's cost grows with its expert's rows; putting the longest
+                // tiles first lets the short ones fill in at the end of the static
+                // round-robin instead of a long tile landing last on one CTA.
+                __syncwarp();
+                int32_t* cnt = ctl->ord_start;
+                for (int b = lane; b < kOrdBuckets; b += 32) cnt[b] = 0;
+                __syncwarp();
+                const unsigned lt = (1u << lane) - 1u;
+                for (int e0 = 0; e0 < p.E; e0 += 32) {
+                    const int e = e0 + lane;
+                    const int b = e < p.E ? expert_size_bucket((s_off[e + 1] - s_off[e] + kBK - 1) / kBK) : -1;
+                    const unsigned peers = __match_any_sync(0xffffffffu, b);
+                    if (b >= 0 && (peers & lt) == 0) cnt[b] += __popc(peers);
+                    __syncwarp();
+                }
+                // exclusive prefix in descending bucket order (4 buckets a lane)
+                int c4[kOrdBuckets / 32], sum = 0;
+#pragma unroll
+                for (int q = 0; q < kOrdBuckets / 32; ++q) {
+                    c4[q] = cnt[kOrdBuckets - 1 - (lane * (kOrdBuckets / 32) + q)];
+                    sum += c4[q];
+                }
+                int incl = sum;
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d) incl += y;
+                }
+                int run = incl - sum;
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < kOrdBuckets / 32; ++q) {
+                    cnt[kOrdBuckets - 1 - (lane * (kOrdBuckets / 32) + q)] = run;
+                    run += c4[q];
+                }
+                __syncwarp();
+                for (int e0 = 0; e0 < p.E; e0 += 32) {
+                    const int e = e0 + lane;
+                    const int b = e < p.E ? expert_size_bucket((s_off[e + 1] - s_off[e] + kBK - 1) / kBK) : -1;
+                    const unsigned peers = __match_any_sync(0xffffffffu, b);
+                    if (b >= 0) s_tp[cnt[b] + __popc(peers & lt)] = e;
+                    __syncwarp();
+                    if (b >= 0 && (peers & lt) == 0) cnt[b] += __popc(peers);
+                    __syncwarp();
+                }
             }
         }
         if (lane == 0) {
