@@ -38,7 +38,8 @@ class TorchDistExchange:
         self.dist.all_to_all_single(out, inp, group=self.group)
 
     def all_to_all(self, out, inp, out_splits, in_splits):
-        self.dist.all_to_all_single(out, inp, list(out_splits), list(in_splits), group=self.group)
+        self.dist.all_to_all_single(out, inp, [int(c) for c in out_splits], [int(c) for c in in_splits],
+                                    group=self.group)
 
 
 def plan(m_sizes, recv_m, G: int, E_loc: int, row_map: bool = False) -> dict:
