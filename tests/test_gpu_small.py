@@ -485,6 +485,73 @@ def test_dual_asym(ta, tb, dims):
     assert_close(hbf(Y1), R1, "dual Y1")
 
 
+def _at_16_byte_offset(*shape):
+    """A NaN-filled bf16 view whose rows start 16 bytes past a 32-byte boundary
+    (the epilogue's 32-byte stores then step down to 16-byte ones), and the
+    whole buffer, to check that nothing outside the view is written."""
+    n = int(np.prod(shape))
+    buf = _nan_filled(n + 16)
+    return buf[8:8 + n].view(*shape), buf
+
+
+def _guard_intact(buf, n):
+    assert torch.isnan(buf[:8].float()).all() and torch.isnan(buf[8 + n:].float()).all()
+
+
+def test_outputs_at_16_byte_offsets_match_aligned_outputs():
+    """Every GEMM output written through rows that are 16- but not 32-byte
+    aligned: bit-identical to the same call into an aligned buffer, equal to
+    the oracle, and nothing written outside the output."""
+    T, topk, E, K, N = 300, 2, 5, 136, 256
+    ids, w, ro = _problem(T, topk, E, K, N, (2,), 91)
+    R = T * topk
+    X = synth.normal_bf16(91, "ox", (R, K), 0.1)
+    W = synth.normal_bf16(92, "ow", (E, N, K), 0.1)
+    dY = synth.normal_bf16(93, "ody", (R, N), 0.1)
+    r = _route_gpu(ids, E)
+    st = status_tensor()
+    m, gi = r["m_sizes"], r["gather_idx"]
+    # forward
+    Y_al = gg.forward(dbf(X), dbf(W), m, gi, None, topk, status=st)
+    Y_off, buf = _at_16_byte_offset(R, N)
+    gg.forward(dbf(X), dbf(W), m, gi, None, topk, out=Y_off, status=st)
+    assert torch.equal(Y_off, Y_al)
+    _guard_intact(buf, R * N)
+    assert_close(hbf(Y_off), orc.forward(X, W, ro["m_sizes"], ro["gather_idx"], None, T, topk, 0, 0, 0),
+                 "forward at a 16-byte offset")
+    # SwiGLU forward: both the pre-activation and the activation outputs offset
+    H_al, A_al = gg.forward_swiglu(dbf(X), dbf(W), m, gi, topk, status=st)
+    H_off, hbuf = _at_16_byte_offset(R, N)
+    A_off, abuf = _at_16_byte_offset(R, N // 2)
+    gg.forward_swiglu(dbf(X), dbf(W), m, gi, topk, out=H_off, out_act=A_off, status=st)
+    assert torch.equal(H_off, H_al) and torch.equal(A_off, A_al)
+    _guard_intact(hbuf, R * N)
+    _guard_intact(abuf, R * N // 2)
+    # dX
+    dX_al = gg.backward_dX(dbf(dY), dbf(W), m, gi, T, topk, status=st)
+    dX_off, xbuf = _at_16_byte_offset(R, K)
+    gg.backward_dX(dbf(dY), dbf(W), m, gi, T, topk, out=dX_off, status=st)
+    assert torch.equal(dX_off, dX_al)
+    _guard_intact(xbuf, R * K)
+    # dW (K = 136: a row pitch of 272 bytes, 16- but not 32-byte aligned, in both buffers)
+    dW_al = gg.backward_dW(dbf(X), dbf(dY), m, gi, T, topk, status=st)
+    dW_off, wbuf = _at_16_byte_offset(E, N, K)
+    gg.backward_dW(dbf(X), dbf(dY), m, gi, T, topk, out=dW_off, status=st)
+    assert torch.equal(dW_off, dW_al)
+    _guard_intact(wbuf, E * N * K)
+    assert_close(hbf(dW_off), orc.backward_dW(X, dY, ro["m_sizes"], ro["gather_idx"], T, topk, 0, 0),
+                 "dW at a 16-byte offset")
+    # the dual GEMM on 2-CTA pairs, one output offset
+    cfg = synth.DualConfig(m0=1032, m1=520, k=136, n0=4104 - 8, n1=768, seed=9)
+    d = synth.dual_tensors(cfg, False, False)
+    Y0_al, Y1_al = gg.dual_asym(dbf(d["X0"]), dbf(d["X1"]), dbf(d["W0"]), dbf(d["W1"]), status=st)
+    Y1_off, dbuf = _at_16_byte_offset(520, 768)
+    Y0, _ = gg.dual_asym(dbf(d["X0"]), dbf(d["X1"]), dbf(d["W0"]), dbf(d["W1"]), out1=Y1_off, status=st)
+    assert torch.equal(Y1_off, Y1_al) and torch.equal(Y0, Y0_al)
+    _guard_intact(dbuf, 520 * 768)
+    assert status_of(st) == 0
+
+
 def test_topk_weights_of_the_wrong_size_are_refused():
     """The C ABI takes a bare pointer to [T, topk] weights; the binding refuses a
     tensor of another size before anything is launched."""

@@ -408,6 +408,14 @@ __device__ __forceinline__ void st_global_16_policy(void* ptr, const uint4& v, u
                  : "memory");
 }
 
+// 32-byte store of a then b (ptr 32-byte aligned), with an L2 policy: one full
+// sector per store, half the store instructions of two 16-byte stores.
+__device__ __forceinline__ void st_global_32_policy(void* ptr, const uint4& a, const uint4& b, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(ptr),
+                 "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w), "l"(pol)
+                 : "memory");
+}
+
 // out[0..7] += v (eight bf16 lanes, each add rounded to bf16), one atomic
 // reduction per 16 bytes; the order of concurrent adds is unspecified.
 __device__ __forceinline__ void red_add_bf16x8(void* ptr, const uint4& v) {

@@ -106,6 +106,11 @@ struct GemmParams {
     uint16_t* act_out;
     int64_t ld_act;
     DualProblem dual[2];
+    // set at launch of a pair kernel: the output rows (act_out's rows) start 32-byte
+    // aligned, so the epilogue stores 32 bytes of a row at a time (st32 also
+    // replaces the shared-memory staging of the pair epilogue)
+    int st32;
+    int act_st32;
     int32_t* status;
 };
 
@@ -847,7 +852,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             // staged stores (below): the destination row pointers of the 8 rows each
             // lane stores, gathered from their owners before the wait, so the work
             // after the accumulator lands is TMEM loads and stores only
-            const bool staged = Tr::kEpiStage && out != nullptr;
+            const bool staged = Tr::kEpiStage && out != nullptr && !p.st32;
             uint8_t* stg = epi_stage + q * 4096;
             uint16_t* drow[8];
             if (staged) {
@@ -917,41 +922,75 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     }
                 }
                 if (orow) {
+                    // eight bf16 of the row, scaled, as one 16-byte piece
+                    auto piece = [&](int pc) {
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(v[pc * 8 + 0]) * sc, __uint_as_float(v[pc * 8 + 1]) * sc);
+                        o.y = pack_bf16x2(__uint_as_float(v[pc * 8 + 2]) * sc, __uint_as_float(v[pc * 8 + 3]) * sc);
+                        o.z = pack_bf16x2(__uint_as_float(v[pc * 8 + 4]) * sc, __uint_as_float(v[pc * 8 + 5]) * sc);
+                        o.w = pack_bf16x2(__uint_as_float(v[pc * 8 + 6]) * sc, __uint_as_float(v[pc * 8 + 7]) * sc);
+                        return o;
+                    };
+                    if constexpr (PAIR) {
+                        // both pieces of a step formed first: one 32-byte store when the
+                        // row is 32-byte aligned (st32) and both are in range
 #pragma unroll
-                    for (int pc = 0; pc < 4; ++pc) {
-                        const int col = col0 + pc * 8;
-                        if (col < ncols) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(v[pc * 8 + 0]) * sc, __uint_as_float(v[pc * 8 + 1]) * sc);
-                            o.y = pack_bf16x2(__uint_as_float(v[pc * 8 + 2]) * sc, __uint_as_float(v[pc * 8 + 3]) * sc);
-                            o.z = pack_bf16x2(__uint_as_float(v[pc * 8 + 4]) * sc, __uint_as_float(v[pc * 8 + 5]) * sc);
-                            o.w = pack_bf16x2(__uint_as_float(v[pc * 8 + 6]) * sc, __uint_as_float(v[pc * 8 + 7]) * sc);
-                            if (KIND == KIND_RAGGED_M && p.combine_out) red_add_bf16x8(orow + col, o);
-                            else st_global_16_policy(orow + col, o, out_pol);
+                        for (int pc = 0; pc < 4; pc += 2) {
+                            const int col = col0 + pc * 8;
+                            const uint4 o0 = piece(pc), o1 = piece(pc + 1);
+                            if (KIND == KIND_RAGGED_M && p.combine_out) {
+                                if (col < ncols) red_add_bf16x8(orow + col, o0);
+                                if (col + 8 < ncols) red_add_bf16x8(orow + col + 8, o1);
+                            } else if (p.st32 && col + 8 < ncols) {
+                                st_global_32_policy(orow + col, o0, o1, out_pol);
+                            } else {
+                                if (col < ncols) st_global_16_policy(orow + col, o0, out_pol);
+                                if (col + 8 < ncols) st_global_16_policy(orow + col + 8, o1, out_pol);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int pc = 0; pc < 4; ++pc) {
+                            const int col = col0 + pc * 8;
+                            if (col < ncols) {
+                                if (KIND == KIND_RAGGED_M && p.combine_out) red_add_bf16x8(orow + col, piece(pc));
+                                else st_global_16_policy(orow + col, piece(pc), out_pol);
+                            }
                         }
                     }
                 }
             };
             auto store_act32 = [&](const uint32_t (&v)[32], int col0) {
                 if (arow_out) {
-                    // 16 gate/up pairs of this chunk -> 16 activations (two 16-byte pieces)
+                    // 16 gate/up pairs of this chunk -> 16 activations (two 16-byte
+                    // pieces; one 32-byte store when act_st32 and both are in range)
+                    auto piece = [&](int pc) {
+                        float a[8];
 #pragma unroll
-                    for (int pc = 0; pc < 2; ++pc) {
-                        if (col0 + pc * 16 < ncols) {
-                            float a[8];
-#pragma unroll
-                            for (int qq = 0; qq < 8; ++qq) {
-                                const float g = __uint_as_float(v[pc * 16 + 2 * qq]);
-                                const float u = __uint_as_float(v[pc * 16 + 2 * qq + 1]);
-                                a[qq] = g / (1.0f + __expf(-g)) * u;
-                            }
-                            uint4 o;
-                            o.x = pack_bf16x2(a[0], a[1]);
-                            o.y = pack_bf16x2(a[2], a[3]);
-                            o.z = pack_bf16x2(a[4], a[5]);
-                            o.w = pack_bf16x2(a[6], a[7]);
-                            st_global_16_policy(arow_out + col0 / 2 + pc * 8, o, out_pol);
+                        for (int qq = 0; qq < 8; ++qq) {
+                            const float g = __uint_as_float(v[pc * 16 + 2 * qq]);
+                            const float u = __uint_as_float(v[pc * 16 + 2 * qq + 1]);
+                            a[qq] = g / (1.0f + __expf(-g)) * u;
                         }
+                        uint4 o;
+                        o.x = pack_bf16x2(a[0], a[1]);
+                        o.y = pack_bf16x2(a[2], a[3]);
+                        o.z = pack_bf16x2(a[4], a[5]);
+                        o.w = pack_bf16x2(a[6], a[7]);
+                        return o;
+                    };
+                    if constexpr (PAIR) {
+                        const uint4 o0 = piece(0), o1 = piece(1);
+                        if (p.act_st32 && col0 + 16 < ncols) {
+                            st_global_32_policy(arow_out + col0 / 2, o0, o1, out_pol);
+                        } else {
+                            if (col0 < ncols) st_global_16_policy(arow_out + col0 / 2, o0, out_pol);
+                            if (col0 + 16 < ncols) st_global_16_policy(arow_out + col0 / 2 + 8, o1, out_pol);
+                        }
+                    } else {
+#pragma unroll
+                        for (int pc = 0; pc < 2; ++pc)
+                            if (col0 + pc * 16 < ncols) st_global_16_policy(arow_out + col0 / 2 + pc * 8, piece(pc), out_pol);
                     }
                 }
             };
@@ -1292,10 +1331,23 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
     }
     const int64_t sms = num_sms();
     if (tile_bound < 1) tile_bound = 1;
+    // 32-byte stores need every destination row 32-byte aligned: the base and the
+    // row pitch (a multiple of 16 bf16)
+    GemmParams q = p;
+    auto rows32 = [](const void* base, int64_t ld) {
+        return base != nullptr && (reinterpret_cast<uintptr_t>(base) & 31u) == 0 && ld % 16 == 0;
+    };
+    if (KIND == KIND_DUAL)
+        q.st32 = (p.dual[0].m == 0 || rows32(p.dual[0].out, p.dual[0].ld_out)) &&
+                 (p.dual[1].m == 0 || rows32(p.dual[1].out, p.dual[1].ld_out));
+    else
+        q.st32 = rows32(p.out, p.ld_out);
+    q.act_st32 = rows32(p.act_out, p.ld_act);
+    if (!PAIR) q.st32 = q.act_st32 = 0;
     clear_pending_launch_error();
     if (!PAIR) {
         const int64_t grid = tile_bound < sms ? tile_bound : sms;
-        kern<<<static_cast<unsigned>(grid), Tr::kThreads, smem, stream>>>(a0, b0, a1, b1, p);
+        kern<<<static_cast<unsigned>(grid), Tr::kThreads, smem, stream>>>(a0, b0, a1, b1, q);
     } else {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
@@ -1323,7 +1375,7 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
         }
         const int64_t clusters = tile_bound < max_clusters[dev] ? tile_bound : max_clusters[dev];
         cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-        e = cudaLaunchKernelEx(&cfg, kern, a0, b0, a1, b1, p);
+        e = cudaLaunchKernelEx(&cfg, kern, a0, b0, a1, b1, q);
         if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
     }
     return launch_result();
