@@ -715,8 +715,12 @@ def run_only(args, cfg):
         return
     if name == "fwd1":
         Xp, W1 = rnd(R, K), rnd(E, N1, K)
-        H, A2 = torch.empty(R, N1, dtype=bf, device=dev), torch.empty(R, I, dtype=bf, device=dev)
-        fn = lambda: gg.forward_swiglu(Xp, W1, m, gi, k, False, out=H, out_act=A2)
+        H = torch.empty(R, N1, dtype=bf, device=dev)
+        if I:
+            A2 = torch.empty(R, I, dtype=bf, device=dev)
+            fn = lambda: gg.forward_swiglu(Xp, W1, m, gi, k, False, out=H, out_act=A2)
+        else:  # a config without the gated MLP (zipf64): the plain forward
+            fn = lambda: gg.forward(Xp, W1, m, gi, None, k, out=H)
     elif name == "fwd2":
         A2, W2 = rnd(R, I), rnd(E, K, I)
         Y2 = torch.empty(R, K, dtype=bf, device=dev)

@@ -102,6 +102,28 @@ size_t gg_workspace_size(int op, int64_t T, int topk, int E, int64_t N, int64_t 
  * word is left as it is.  No counterpart on the pages. */
 int gg_read_status(const int32_t* status, int32_t* code, void* stream);
 
+/* Tile schedule of the grouped-GEMM launches (process-wide; returns the
+ * previous mode, or GG_ERR_INVALID_ARG for an unknown one).
+ *   GG_SCHEDULE_AUTO (default): 2-CTA launches over experts whose tiles are
+ *     long (at least 48 reduction blocks of 64 a tile; dW: a mean expert of
+ *     at least 32 blocks) hand tiles out dynamically, from a device counter
+ *     in tile order, so the pairs that read one operand tile read it at about
+ *     the same time and DRAM sees it once; shorter tiles keep the static
+ *     round-robin (pair p takes tiles p, p + P, ...).
+ *   GG_SCHEDULE_STATIC, GG_SCHEDULE_DYNAMIC: always that schedule (dynamic
+ *     only where the launch supports it; the dual GEMM is always static).
+ * Results are identical bit for bit under either schedule: a tile's sums
+ * do not depend on which pair computes it.  The dynamic schedule uses one of
+ * 1024 device counter pairs per launch, in turn, reset by the launch itself
+ * as it ends: more than 1023 dynamic launches in flight at once on one
+ * device (streams that run concurrently, or replays of one captured graph
+ * running concurrently with themselves) is not supported.  No counterpart
+ * on the pages. */
+#define GG_SCHEDULE_AUTO 0
+#define GG_SCHEDULE_STATIC 1
+#define GG_SCHEDULE_DYNAMIC 2
+int gg_set_gemm_schedule(int mode);
+
 /* Diagnostic: runs, in one CTA, the bounded mbarrier wait that every
  * pipelined kernel of this library uses, on a barrier phase nothing ever
  * completes, with a limit of limit_ns (0 < limit_ns <= 2 s).  The wait gives

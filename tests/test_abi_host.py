@@ -131,6 +131,18 @@ def test_host_validation_codes(lib):
     assert L.gg_route_hist_offsets(fake, 64, 2, 4, 8, fake, fake, None, fake, fake, fake, ws, None, None) == _lib.GG_ERR_INVALID_ARG
 
 
+def test_gemm_schedule_mode(lib):
+    """gg_set_gemm_schedule returns the previous mode and refuses unknown ones
+    (host state only: nothing is launched)."""
+    from unpermute_route_hist_gb300 import _lib
+    prev = lib.gg_set_gemm_schedule(_lib.GG_SCHEDULE_STATIC)
+    assert prev == _lib.GG_SCHEDULE_AUTO
+    assert lib.gg_set_gemm_schedule(_lib.GG_SCHEDULE_DYNAMIC) == _lib.GG_SCHEDULE_STATIC
+    assert lib.gg_set_gemm_schedule(3) == _lib.GG_ERR_INVALID_ARG
+    assert lib.gg_set_gemm_schedule(-1) == _lib.GG_ERR_INVALID_ARG
+    assert lib.gg_set_gemm_schedule(_lib.GG_SCHEDULE_AUTO) == _lib.GG_SCHEDULE_DYNAMIC
+
+
 def test_product_path_fails_loudly_without_library(tmp_path, monkeypatch):
     from unpermute_route_hist_gb300 import _lib
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -25,6 +25,7 @@ SIGNATURES = {
     "gg_last_cuda_error": (_cstr, []),
     "gg_workspace_size": (_sz, [_int, _i64, _int, _int, _i64, _i64, _int]),
     "gg_read_status": (_int, [_vp, _vp, _vp]),
+    "gg_set_gemm_schedule": (_int, [_int]),
     "gg_selftest_bounded_wait": (_int, [_vp, _vp, ctypes.c_uint64, _vp]),
     "gg_route_workspace_size": (_sz, [_i64, _int, _int]),
     "gg_route_hist_offsets": (_int, [_vp, _i64, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -74,6 +75,9 @@ GG_OP_BACKWARD_DW = 2
 GG_OP_FORWARD_COMBINE = 3
 GG_PERMUTE_X = 1
 GG_PERMUTE_Y = 2
+GG_SCHEDULE_AUTO = 0
+GG_SCHEDULE_STATIC = 1
+GG_SCHEDULE_DYNAMIC = 2
 
 _lock = threading.Lock()
 _lib = None

@@ -55,6 +55,14 @@ def workspace_size(op: int, T: int, topk: int, E: int, N: int = 0, K: int = 0, f
     return int(_lib.load().gg_workspace_size(op, T, topk, E, N, K, flags))
 
 
+def set_gemm_schedule(mode: int) -> int:
+    """Process-wide tile schedule of the GEMM launches (_lib.GG_SCHEDULE_*); returns the previous mode."""
+    rc = _lib.load().gg_set_gemm_schedule(int(mode))
+    if rc < 0:
+        _lib.check("gg_set_gemm_schedule", rc)
+    return rc
+
+
 def read_status(status):
     """(rc, code): synchronise the current stream, read the device status word;
     rc is GG_OK, GG_ERR_DEVICE_CHECK or GG_ERR_TIMEOUT, code the GG_DEV_* value."""

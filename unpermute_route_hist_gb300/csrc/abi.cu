@@ -6,6 +6,7 @@
 
 #include <cstdio>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -145,6 +146,8 @@ __global__ void selftest_wait_kernel(int32_t* status, uint64_t limit_ns, int32_t
     }
 }
 }  // namespace
+
+std::atomic<int> g_gemm_schedule{GG_SCHEDULE_AUTO};
 }  // namespace gg
 
 using namespace gg;
@@ -207,6 +210,12 @@ int gg_read_status(const int32_t* status, int32_t* code, void* stream) {
     if (code) *code = v;
     if (v == GG_DEV_OK) return GG_OK;
     return v == GG_DEV_TIMEOUT ? GG_ERR_TIMEOUT : GG_ERR_DEVICE_CHECK;
+}
+
+int gg_set_gemm_schedule(int mode) {
+    if (mode != GG_SCHEDULE_AUTO && mode != GG_SCHEDULE_STATIC && mode != GG_SCHEDULE_DYNAMIC)
+        return GG_ERR_INVALID_ARG;
+    return g_gemm_schedule.exchange(mode);
 }
 
 int gg_route_hist_offsets(const int32_t* topk_ids, int64_t T, int topk, int E, int pad_block,

@@ -222,6 +222,24 @@ __device__ __forceinline__ void mbar_arrive_remote(uint64_t* bar, uint32_t cta) 
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(cta));
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
+// Relaxed arrival on the mbarrier at the same offset in CTA `cta`: a count only,
+// ordering nothing (a hand-off whose data travels another way, or none).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+// Hand a 32-bit value to CTA `cta` of the cluster: an asynchronous store into its
+// shared memory (the variable at the same offset as `p`) that completes 4
+// transaction bytes on its mbarrier at the same offset as `bar`, plus that
+// barrier's one arrival with the 4 bytes expected.  A waiter on the barrier sees
+// the value once the phase completes; no cluster-scope fence is involved.
+__device__ __forceinline__ void st_async_u32_signal(const void* p, const uint64_t* bar, uint32_t cta, uint32_t v) {
+    uint32_t rp, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rp) : "r"(smem_u32(p)), "r"(cta));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(bar)), "r"(cta));
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], 4;" ::"r"(rb) : "memory");
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(rp), "r"(v), "r"(rb)
+                 : "memory");
+}
 // Shared::cluster address of the variable at the same offset in CTA `cta`.
 __device__ __forceinline__ uint32_t mapa_u32(const void* p, uint32_t cta) {
     uint32_t remote;

@@ -54,6 +54,10 @@ constexpr int kABytes = kBM * kBK * 2;
 constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators
 constexpr int kGroupM = 16;             // m-tiles per raster group (L2 reuse)
 constexpr int kGatherWarps = 4;
+constexpr int kTQ = 8;                  // tile-queue entries (dynamic schedule)
+constexpr int kSchedSlots = 1024;       // device tile counters, taken in turn by launches
+constexpr int kDynMinBlocksM = 48;      // dynamic schedule from this many reduction blocks a tile
+constexpr int kDynMinBlocksK = 32;      // (RAGGED_K: of the mean expert)
 
 enum GemmKind { KIND_RAGGED_M = 0, KIND_RAGGED_K = 1, KIND_DUAL = 2 };
 // Row index of a gathered operand row for expert-order row i.
@@ -111,6 +115,10 @@ struct GemmParams {
     // replaces the shared-memory staging of the pair epilogue)
     int st32;
     int act_st32;
+    // dynamic schedule (pair kernels with ragged rows or reductions): this launch's
+    // counters {tiles handed out past the first wave, pairs finished}, zero at
+    // launch and reset to zero by the last pair to finish
+    uint32_t* sched;
     int32_t* status;
 };
 
@@ -148,7 +156,22 @@ struct SharedCtl {
     int bad_sizes;
     int64_t total_tiles;
     int32_t ord_start[kOrdBuckets];  // RAGGED_K: expert-order counting sort (prologue only)
+    // dynamic schedule: the even CTA's producer writes tile numbers into tq of both
+    // CTAs (tq_full: one arrival; in the odd CTA also the 4 bytes of an asynchronous
+    // remote store); every reader of both CTAs acknowledges an entry on the even
+    // CTA's tq_empty before it is rewritten
+    int32_t tq[kTQ];
+    uint64_t tq_full[kTQ];
+    uint64_t tq_empty[kTQ];
 };
+
+// Process-wide tile schedule mode (GG_SCHEDULE_*), set by gg_set_gemm_schedule.
+extern std::atomic<int> g_gemm_schedule;
+
+// One device's tile counters for the dynamic schedule, two words a launch slot.
+static __device__ uint32_t g_sched[2 * kSchedSlots];
+// Next launch slot, per device index.
+static std::atomic<uint32_t> g_sched_next[64];
 
 // Tiles are scheduled in "units": one m-tile, or (PAIR) two adjacent m-tiles
 // of the same expert / problem and n-tile that a 2-CTA cluster computes
@@ -286,10 +309,21 @@ struct GemmTraits {
     // (4 KB a warp) so that global stores go out as whole 128-byte row segments (dW's
     // tiles, long reductions sharing shared-memory bandwidth, measured faster without)
     static constexpr bool kEpiStage = PAIR && KIND == KIND_RAGGED_M;
+    // Pair kernels over experts can take tiles from a device counter after the
+    // first wave, in tile order, so the pairs that read the same operand tile read
+    // it at about the same time (a static round-robin lets them drift apart, and
+    // the tile is fetched from DRAM again).  The launch chooses (GemmParams.sched);
+    // the dual GEMM keeps the static schedule.
+    static constexpr bool kDynSched = PAIR && KIND != KIND_DUAL;
+    // readers of a tile-queue entry: even CTA: MMA issuer, 4 epilogue warps (+ the
+    // dW tail helper); odd CTA: producer, 4 epilogue warps (+ the tail helper)
+    static constexpr int kTqReaders = 10 + (kTailBuf ? 2 : 0);
     static_assert(kStages <= kMaxStages, "stage ring");
 };
 
-constexpr int kEpiStageBytes = 4 * 4096;  // 4 epilogue warps x 32 rows x 128 B
+// per epilogue warp: 32 rows x 128 B of staged output, then the 32 rows' destination pointers
+constexpr int kEpiWarpBytes = 4096 + 32 * 8;
+constexpr int kEpiStageBytes = 4 * kEpiWarpBytes;
 
 template <bool PAIR>
 __host__ __device__ constexpr size_t gemm_smem_bytes(int E) {
@@ -324,7 +358,9 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t tile_addr, int ks) {
     }
 }
 
-template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR>
+// DYN: the dynamic tile schedule (a separate instantiation, so the static one
+// carries none of its code).
+template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR, bool DYN>
 __global__ void __launch_bounds__((GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>::kThreads), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
@@ -364,6 +400,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         mbar_init(&ctl->tfull, 1);
         mbar_init(&ctl->pfull, 2);  // the two CTAs' tail helpers
         mbar_init(&ctl->tempty, 1);
+        if (DYN) {
+            for (int j = 0; j < kTQ; ++j) {
+                mbar_init(&ctl->tq_full[j], 1);
+                mbar_init(&ctl->tq_empty[j], Tr::kTqReaders);
+            }
+        }
         ctl->abort_flag = 0;
         fence_barrier_init();
     }
@@ -501,6 +543,63 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     const int64_t total_tiles = ctl->total_tiles;
     const uint32_t stage0 = smem_u32(stage_base);
 
+    // ---------------------------------------------------- tile sequence --
+    // Tile k of this CTA's sequence, -1 past the end.  Static schedule: slot +
+    // k * nslot.  Dynamic: entry k of the tile queue (one thread per reading role
+    // calls it, for every k in turn); the entry is acknowledged on the even CTA's
+    // tq_empty as soon as it is read.
+    auto ack_entry = [&](int j, int32_t t) {
+        if (leader) {
+            mbar_arrive(&ctl->tq_empty[j]);
+        } else {
+            // the arrival's address depends on the value read, so the read has
+            // completed before the even CTA can see the arrival and rewrite the entry
+            uint32_t remote = mapa_u32(&ctl->tq_empty[j], 0);
+            uint32_t z;
+            asm volatile("and.b32 %0, %1, 0;" : "=r"(z) : "r"(t));
+            mbar_arrive_remote_relaxed(remote + z);
+        }
+    };
+    static_assert(!DYN || Tr::kDynSched, "dynamic schedule: pair kernels over experts");
+    constexpr bool dyn = DYN;
+    auto read_tile = [&](int k) -> int32_t {
+        if (!dyn) {
+            const int64_t t = slot + k * nslot;
+            return t < total_tiles ? static_cast<int32_t>(t) : -1;
+        } else {
+            const int j = k % kTQ;
+            const uint32_t par = static_cast<uint32_t>(k / kTQ) & 1u;
+            if (!mbar_wait(&ctl->tq_full[j], par, abort_flag, p.status)) return -1;
+            const int32_t t = *reinterpret_cast<volatile int32_t*>(&ctl->tq[j]);
+            ack_entry(j, t);
+            return t;
+        }
+    };
+    // As read_tile, but only if entry k is already there (the MMA issuer looks
+    // ahead with it and must not block while its own tile is in flight).
+    auto try_read_tile = [&](int k, int32_t& t) -> bool {
+        if (!dyn) {
+            const int64_t ts = slot + k * nslot;
+            t = ts < total_tiles ? static_cast<int32_t>(ts) : -1;
+            return true;
+        } else {
+            const int j = k % kTQ;
+            const uint32_t par = static_cast<uint32_t>(k / kTQ) & 1u;
+            if (!mbar_try_wait(&ctl->tq_full[j], par)) return false;
+            const int32_t v = *reinterpret_cast<volatile int32_t*>(&ctl->tq[j]);
+            ack_entry(j, v);
+            t = v;
+            return true;
+        }
+    };
+    // warp-uniform read_tile (lane 0 reads, every lane gets the tile)
+    auto read_tile_warp = [&](int k) -> int32_t {
+        if (!dyn) return read_tile(k);
+        int32_t t = 0;
+        if (lane == 0) t = read_tile(k);
+        return __shfl_sync(0xffffffffu, t, 0);
+    };
+
     // Rows [valid, zr_end) of a stage's dense operands hold the next expert's
     // reduction rows: overwrite them with zeros (both operands, so no 0 * inf).
     auto zero_tail = [&](int stage, int valid, int zr_end) {
@@ -533,7 +632,46 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             int64_t issued = 0;
             uint32_t tail_uses = 0;  // PAIR dW: tail blocks issued so far
             bool ok = true;
-            for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
+            // dynamic schedule: the even CTA's producer takes the tiles (its first
+            // tile is its slot, later ones come from the launch's counter) and
+            // writes each into the tile queue of both CTAs
+            const bool writer = dyn && leader;
+            bool pub_ok = true;
+            auto publish = [&](int k, int32_t tv) -> bool {
+                const int j = k % kTQ;
+                const uint32_t par = static_cast<uint32_t>(k / kTQ) & 1u;
+                if (!mbar_wait(&ctl->tq_empty[j], par ^ 1u, abort_flag, p.status)) return false;
+                *reinterpret_cast<volatile int32_t*>(&ctl->tq[j]) = tv;
+                mbar_arrive(&ctl->tq_full[j]);
+                st_async_u32_signal(&ctl->tq[j], &ctl->tq_full[j], 1, static_cast<uint32_t>(tv));
+                return true;
+            };
+            int32_t t = writer ? (slot < total_tiles ? static_cast<int32_t>(slot) : -1) : read_tile(0);
+            int npub = 0;  // entries the writer has published
+            if (writer) {
+                if (publish(0, static_cast<int32_t>(t))) ++npub;
+                else { ok = pub_ok = false; t = -1; }
+            }
+            // The writer asks the counter two tiles ahead (the reply for entry k+1 was
+            // asked for as tile k-1 started) and publishes entry k+1 a few blocks into
+            // tile k: the counter's latency stays hidden, and the readers (the odd
+            // CTA's producer above all) find the entry well before they need it.
+            uint32_t g = 0;
+            if (writer && t >= 0) g = atomicAdd(p.sched, 1u);
+            for (int k = 0; t >= 0; ++k) {
+                int32_t t_next = -1;
+                bool next_known = !writer;
+                uint32_t g_after = 0;
+                if (writer) g_after = atomicAdd(p.sched, 1u);
+                auto publish_next = [&]() -> bool {
+                    if (next_known) return true;
+                    next_known = true;
+                    const int64_t tn = nslot + static_cast<int64_t>(g);
+                    t_next = tn < total_tiles ? static_cast<int32_t>(tn) : -1;
+                    if (!publish(k + 1, static_cast<int32_t>(t_next))) { pub_ok = false; return false; }
+                    ++npub;
+                    return true;
+                };
                 const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
                 const CUtensorMap* mA = (KIND == KIND_DUAL && ti.e == 1) ? &tmA1 : &tmA0;
                 const CUtensorMap* mB = (KIND == KIND_DUAL && ti.e == 1) ? &tmB1 : &tmB0;
@@ -626,6 +764,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     }
                     ++issued;
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    if (writer && kb == 2 && !publish_next()) { ok = false; break; }
+                }
+                if (!ok) break;
+                if (writer) {
+                    if (!publish_next()) { ok = false; break; }
+                    t = t_next;
+                    g = g_after;
+                } else {
+                    t = read_tile(k + 1);
+                }
+            }
+            if (writer) {
+                // a producer that gave up still ends its readers' sequences
+                if (!ok && pub_ok) publish(npub, -1);
+                // This pair takes no more tiles.  The last pair to get here has seen
+                // every pair's last request (each precedes its pair's count), so it
+                // can reset the counters for the next launch that uses them.
+                uint32_t old;
+                asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.sched + 1) : "memory");
+                if (old == static_cast<uint32_t>(nslot) - 1u) {
+                    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p.sched), "r"(0u) : "memory");
+                    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p.sched + 1), "r"(0u) : "memory");
                 }
             }
             // Let every TMA copy this thread issued land before the CTA can exit.
@@ -658,17 +818,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 bool ok = true, any_mma = false;
                 // The next tile is decoded right after this tile's first MMAs are
                 // issued, while the tensor core works on them, instead of at the
-                // tile boundary, where the issuer may be the critical path.
-                TileInfo ti_next = slot < total_tiles ? decode_tile<KIND, PAIR>(slot, p, s_off, s_tp, rank) : TileInfo{};
-                for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
+                // tile boundary, where the issuer may be the critical path.  (With
+                // the dynamic schedule only if its number is already in the queue:
+                // the entry may wait for this tile's loads, so the issuer blocks on
+                // it only at the tile's end.)
+                int32_t t = read_tile(0);
+                TileInfo ti_next = t >= 0 ? decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank) : TileInfo{};
+                int32_t t_next = -1;
+                for (int k = 0; t >= 0 && ok; ++k, t = t_next) {
                     const TileInfo ti = ti_next;
                     bool next_decoded = false;
-                    auto decode_next = [&]() {
+                    auto decode_next = [&](bool block) {
                         if (next_decoded) return;
+                        if (block) t_next = read_tile(k + 1);
+                        else if (!try_read_tile(k + 1, t_next)) return;
                         next_decoded = true;
-                        if (t + nslot < total_tiles) ti_next = decode_tile<KIND, PAIR>(t + nslot, p, s_off, s_tp, rank);
+                        if (t_next >= 0) ti_next = decode_tile<KIND, PAIR>(t_next, p, s_off, s_tp, rank);
                     };
-                    if (ti.nkb == 0) { decode_next(); continue; }
+                    if (ti.nkb == 0) { decode_next(true); continue; }
                     const uint32_t buf = acc_count & 1u;
                     const uint32_t acc_phase = (acc_count >> 1) & 1u;
                     if (!mbar_wait(&ctl->tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.status, 0, kWaitLimitNs, PAIR)) {
@@ -708,7 +875,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     // for the decode
                     if (nfull > 0) {
                         if (!issue_block(0)) { ok = false; break; }
-                        decode_next();
+                        decode_next(false);
                     }
                     for (int kb = 1; kb < nfull; ++kb)
                         if (!issue_block(kb)) { ok = false; break; }
@@ -731,7 +898,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         umma_commit_pair(&ctl->tempty, 0x3);  // the tail buffer is free in both CTAs
                         any_mma = true;
                     }
-                    decode_next();  // (a tile of only a tail block has not decoded it yet)
+                    decode_next(true);
                     if (PAIR) umma_commit_pair(&ctl->tmem_full[buf], 0x3);
                     else umma_commit(&ctl->tmem_full[buf]);
                     ++acc_count;
@@ -808,7 +975,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         const uint64_t out_pol = l2_policy_evict_first();
         const int r = q * 32 + lane;   // tile row of this thread
         uint32_t acc_count = 0;
-        for (int64_t t = slot; t < total_tiles; t += nslot) {
+        int64_t t_static = slot;  // static schedule: this CTA's next tile
+        for (int k = 0;; ++k) {
+            int64_t t;
+            if constexpr (DYN) {
+                t = read_tile_warp(k);
+                if (t < 0) break;
+            } else {
+                t = t_static;
+                if (t >= total_tiles) break;
+                t_static += nslot;
+            }
             // (PAIR: an odd CTA past its expert's last m-tile has rows <= 0; it
             // still takes part in the accumulator hand-off but stores nothing.)
             const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
@@ -849,21 +1026,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 }
                 continue;
             }
-            // staged stores (below): the destination row pointers of the 8 rows each
-            // lane stores, gathered from their owners before the wait, so the work
-            // after the accumulator lands is TMEM loads and stores only
+            // staged stores (below): every row's destination pointer goes to shared
+            // memory before the wait (its index load completes meanwhile), where the
+            // lanes storing that row read it; the work after the accumulator lands
+            // is TMEM loads and stores only
             const bool staged = Tr::kEpiStage && out != nullptr && !p.st32;
-            uint8_t* stg = epi_stage + q * 4096;
-            uint16_t* drow[8];
+            uint8_t* stg = epi_stage + q * kEpiWarpBytes;
+            uint16_t** srow = reinterpret_cast<uint16_t**>(stg + 4096);
             if (staged) {
-                const uint64_t mine = reinterpret_cast<uint64_t>(orow);
-#pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int src = (lane >> 3) + 4 * it;
-                    const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(mine), src);
-                    const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(mine >> 32), src);
-                    drow[it] = reinterpret_cast<uint16_t*>((static_cast<uint64_t>(hi) << 32) | lo);
-                }
+                srow[lane] = orow;
+                __syncwarp();
             }
             // SwiGLU backward (dX with the stored H): this row's H values for the first
             // kHAhead 16-column steps are loaded before the accumulator lands; each
@@ -1025,9 +1197,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 }
 #pragma unroll
                 for (int it = 0; it < 8; ++it) {
-                    if (drow[it] && col < ncols) {
-                        if (KIND == KIND_RAGGED_M && p.combine_out) red_add_bf16x8(drow[it] + col, o[it]);
-                        else st_global_16_policy(drow[it] + col, o[it], out_pol);
+                    uint16_t* dr = srow[(lane >> 3) + 4 * it];
+                    if (dr && col < ncols) {
+                        if (KIND == KIND_RAGGED_M && p.combine_out) red_add_bf16x8(dr + col, o[it]);
+                        else st_global_16_policy(dr + col, o[it], out_pol);
                     }
                 }
                 __syncwarp();
@@ -1132,7 +1305,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         // loaded a few stages into the tile and is consumed at its end, so this
         // work overlaps the tile's main loop.
         uint32_t tail_uses = 0;
-        for (int64_t t = slot; t < total_tiles; t += nslot) {
+        for (int k = 0;; ++k) {
+            const int32_t t = read_tile_warp(k);
+            if (t < 0) break;
             const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
             const int nfull = ti.red_len / kBK;
             if (nfull == ti.nkb) continue;
@@ -1314,21 +1489,11 @@ template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAI
 int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
                 const CUtensorMap& b1, const GemmParams& p, int64_t tile_bound, cudaStream_t stream) {
     using Tr = GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>;
-    auto kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>;
     const size_t smem = gemm_smem_bytes<PAIR>(p.E);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
     if (dev < 0 || dev >= 64) dev = 0;
-    // the shared-memory opt-in is set once per kernel and device (host overhead
-    // matters for small launches)
-    static std::atomic<bool> smem_set[64];
-    if (!smem_set[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(gemm_smem_bytes<PAIR>(GG_MAX_EXPERTS)));
-        if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
-        smem_set[dev].store(true, std::memory_order_release);
-    }
     const int64_t sms = num_sms();
     if (tile_bound < 1) tile_bound = 1;
     // 32-byte stores need every destination row 32-byte aligned: the base and the
@@ -1344,6 +1509,42 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
         q.st32 = rows32(p.out, p.ld_out);
     q.act_st32 = rows32(p.act_out, p.ld_act);
     if (!PAIR) q.st32 = q.act_st32 = 0;
+    // Dynamic schedule for long tiles: its hand-off costs a few hundred cycles a
+    // tile, and lock-step co-readers of short tiles meet their DRAM misses all at
+    // once, so short tiles keep the static round-robin (measured: dynamic wins
+    // 1-4% at 64-448 reduction blocks a tile and loses 2-6% at 12-24).  RAGGED_K:
+    // the mean expert's reduction length.  This launch's pair of tile counters is
+    // taken in turn; tile numbers travel as 32-bit values.
+    q.sched = nullptr;
+    const int64_t mean_blocks = KIND == KIND_RAGGED_K ? p.R / (kBK * (p.E > 0 ? p.E : 1)) : p.Kred / kBK;
+    const int mode = g_gemm_schedule.load(std::memory_order_relaxed);
+    const bool dyn = mode == GG_SCHEDULE_DYNAMIC ||
+                     (mode == GG_SCHEDULE_AUTO && mean_blocks >= (KIND == KIND_RAGGED_K ? kDynMinBlocksK : kDynMinBlocksM));
+    if (Tr::kDynSched && dyn) {
+        if (tile_bound > (int64_t(1) << 30)) return GG_ERR_UNSUPPORTED;
+        static std::atomic<void*> sched_base[64];
+        void* base = sched_base[dev].load(std::memory_order_acquire);
+        if (!base) {
+            e = cudaGetSymbolAddress(&base, g_sched);
+            if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+            sched_base[dev].store(base, std::memory_order_release);
+        }
+        const uint32_t s = g_sched_next[dev].fetch_add(1u, std::memory_order_relaxed) % kSchedSlots;
+        q.sched = static_cast<uint32_t*>(base) + 2 * s;
+    }
+    auto kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR, false>;
+    if constexpr (Tr::kDynSched)
+        if (q.sched) kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR, true>;
+    // the shared-memory opt-in is set once per kernel and device (host overhead
+    // matters for small launches)
+    static std::atomic<bool> smem_set[2][64];
+    const int kid = q.sched ? 1 : 0;
+    if (!smem_set[kid][dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(gemm_smem_bytes<PAIR>(GG_MAX_EXPERTS)));
+        if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
+        smem_set[kid][dev].store(true, std::memory_order_release);
+    }
     clear_pending_launch_error();
     if (!PAIR) {
         const int64_t grid = tile_bound < sms ? tile_bound : sms;
@@ -1362,6 +1563,7 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
         cfg.numAttrs = 1;
         // as many 2-CTA clusters as can be resident at once (a GPC with an odd
         // SM count leaves an SM out), at most one per tile pair
+        // (the same for both schedules' kernels: same block, registers and shared memory)
         static int max_clusters[64] = {0};
         if (max_clusters[dev] == 0) {
             cfg.gridDim = dim3(static_cast<unsigned>(sms & ~int64_t(1)));
