@@ -463,9 +463,10 @@ def run_gg(args, cfg):
 
     # ---- end to end through the public API with host buffers ------------------
     # Every step uploads its inputs from pinned host memory and reads its two
-    # [T, K] results back.  Two buffer sets and a copy stream let step i+1's
-    # upload and step i's download run while the GPU computes; the timed region
-    # runs from the first upload to the last download.
+    # [T, K] results back.  Two buffer sets and one copy stream per direction let
+    # step i+1's upload and step i's download run while the GPU computes (and at
+    # the same time as each other: the link carries both directions at once);
+    # the timed region runs from the first upload to the last download.
     pin = {n: pinned(v) for n, v in inputs_host.items()}
     pin_ids = torch.from_numpy(host["ids"]).pin_memory()
     pin_w = torch.from_numpy(host["w"]).pin_memory()
@@ -473,28 +474,42 @@ def run_gg(args, cfg):
     d2h = 2 * T * K * 2
     # as many steps as the device-timed region: both are sustained under the power cap
     e_steps = max(2, args.steps)
-    copy_stream = torch.cuda.Stream(dev)
+    up_stream, down_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     srcs = [src, {n: torch.empty_like(v) for n, v in src.items()}]
     resd = [{"out": out, "dXt": dXt}, {"out": torch.empty_like(out), "dXt": torch.empty_like(dXt)}]
     res_host = [[torch.empty(T, K, dtype=bf).pin_memory() for _ in range(2)] for _ in range(2)]
     h2d_ev = [torch.cuda.Event() for _ in range(2)]
     comp_ev = [torch.cuda.Event() for _ in range(2)]
     d2h_ev = [torch.cuda.Event() for _ in range(2)]
+    # copy durations (timed events around each copy; reported as a diagnostic)
+    cp_ev = {"h2d": [], "d2h": []}
+
+    def timed_copy(kind, strm, fn):
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(strm)
+        fn()
+        b_.record(strm)
+        cp_ev[kind].append((a, b_))
 
     def upload(b):
-        with torch.cuda.stream(copy_stream):
-            for n in pin:
-                srcs[b][n].copy_(pin[n], non_blocking=True)
-            srcs[b]["ids"].copy_(pin_ids, non_blocking=True)
-            srcs[b]["w"].copy_(pin_w, non_blocking=True)
-            h2d_ev[b].record(copy_stream)
+        with torch.cuda.stream(up_stream):
+            def go():
+                for n in pin:
+                    srcs[b][n].copy_(pin[n], non_blocking=True)
+                srcs[b]["ids"].copy_(pin_ids, non_blocking=True)
+                srcs[b]["w"].copy_(pin_w, non_blocking=True)
+            timed_copy("h2d", up_stream, go)
+            h2d_ev[b].record(up_stream)
 
     def download(b):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(comp_ev[b])
-            res_host[b][0].copy_(resd[b]["out"], non_blocking=True)
-            res_host[b][1].copy_(resd[b]["dXt"], non_blocking=True)
-            d2h_ev[b].record(copy_stream)
+        with torch.cuda.stream(down_stream):
+            down_stream.wait_event(comp_ev[b])
+
+            def go():
+                res_host[b][0].copy_(resd[b]["out"], non_blocking=True)
+                res_host[b][1].copy_(resd[b]["dXt"], non_blocking=True)
+            timed_copy("d2h", down_stream, go)
+            d2h_ev[b].record(down_stream)
 
     def e2e_run(n, cevs=None):
         upload(0)
@@ -511,7 +526,7 @@ def run_gg(args, cfg):
             comp_ev[b].record(stream)
             if i + 1 < n:
                 if i >= 1:
-                    copy_stream.wait_event(comp_ev[1 - b])  # step i-1 done with its inputs
+                    up_stream.wait_event(comp_ev[1 - b])  # step i-1 done with its inputs
                 upload(1 - b)
             download(b)
 
@@ -527,10 +542,13 @@ def run_gg(args, cfg):
     e_clocks = Clocks(local)
     e_clocks.start()
     time.sleep(0.3)
-    e0.record(copy_stream)
+    for v in cp_ev.values():
+        v.clear()
+    e0.record(up_stream)
     e2e_run(e_steps, cevs)
-    e1.record(copy_stream)
+    e1.record(down_stream)  # after the last download, which follows every step and upload
     torch.cuda.synchronize()
+    copy_ms = {k: statistics.median(a.elapsed_time(b_) for a, b_ in v) for k, v in cp_ev.items()}
     e_clk = e_clocks.stop()
     e_compute_ms = sum(a.elapsed_time(b) for a, b in cevs) / e_steps
     e_ms, e_value = aggregate_step_time(e0.elapsed_time(e1) / e_steps, step_flops, ws,
@@ -641,7 +659,8 @@ def run_gg(args, cfg):
             "variants": variants,
             "e2e": {"value": e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms,
-                    "compute_ms_per_step": e_compute_ms, "steps": e_steps, "clocks": e_clk},
+                    "compute_ms_per_step": e_compute_ms, "copy_ms": copy_ms, "steps": e_steps,
+                    "clocks": e_clk},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
