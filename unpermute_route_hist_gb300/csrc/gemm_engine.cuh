@@ -569,7 +569,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         } else {
             const int j = k % kTQ;
             const uint32_t par = static_cast<uint32_t>(k / kTQ) & 1u;
-            if (!mbar_wait(&ctl->tq_full[j], par, abort_flag, p.status)) return -1;
+            // (odd CTA: a cluster-scope acquire, pairing with the release of the even
+            // CTA's remote store completing on this barrier)
+            if (!mbar_wait(&ctl->tq_full[j], par, abort_flag, p.status, 0, kWaitLimitNs, !leader)) return -1;
             const int32_t t = *reinterpret_cast<volatile int32_t*>(&ctl->tq[j]);
             ack_entry(j, t);
             return t;
@@ -585,7 +587,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         } else {
             const int j = k % kTQ;
             const uint32_t par = static_cast<uint32_t>(k / kTQ) & 1u;
-            if (!mbar_try_wait(&ctl->tq_full[j], par)) return false;
+            if (!(leader ? mbar_try_wait(&ctl->tq_full[j], par) : mbar_try_wait_cluster(&ctl->tq_full[j], par)))
+                return false;
             const int32_t v = *reinterpret_cast<volatile int32_t*>(&ctl->tq[j]);
             ack_entry(j, v);
             t = v;
