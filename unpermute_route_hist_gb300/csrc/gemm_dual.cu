@@ -9,7 +9,8 @@
 // CTA loading its own rows and half of the 256 columns, so each SM's operand
 // stream is a third smaller (8192 x 8192 rows: 1258 -> 1486 TFLOP/s).  A
 // problem that fits one wave keeps single-CTA tiles, which start ~1 us sooner
-// (the stated 512/256-row shape: 9.8 us against 10.8 us on pairs).
+// (the stated 512/256-row shape: 9.8 us against 10.8 us on pairs), and one that
+// fits a wave even in 128 x 128 tiles runs those, over twice as many SMs.
 #include "gemm_engine.cuh"
 
 using namespace gg;
@@ -51,7 +52,12 @@ extern "C" int gg_dual_asym(const gg_bf16* X0, const gg_bf16* X1, const gg_bf16*
     p.dual[1] = DualProblem{e1 ? 0 : static_cast<int>(m1), e1 ? 0 : static_cast<int>(n1), Y1, n1};
     const int64_t single_tiles = ((m0 + kBM - 1) / kBM) * ((n0 + kBN - 1) / kBN) +
                                  ((m1 + kBM - 1) / kBM) * ((n1 + kBN - 1) / kBN);
+    const int64_t narrow_tiles = ((m0 + kBM - 1) / kBM) * ((n0 + kBN / 2 - 1) / (kBN / 2)) +
+                                 ((m1 + kBM - 1) / kBM) * ((n1 + kBN / 2 - 1) / (kBN / 2));
     const bool pair = single_tiles > num_sms();
+    // one wave even in 128 x 128 tiles: those, so twice as many SMs share the work
+    const bool narrow = !pair && narrow_tiles <= num_sms();
+    p.narrow = narrow ? 1 : 0;
     CUtensorMap mA[2], mB[2];
     const gg_bf16* Xs[2] = {X0, X1};
     const gg_bf16* Ws[2] = {W0, W1};
@@ -62,18 +68,19 @@ extern "C" int gg_dual_asym(const gg_bf16* X0, const gg_bf16* X1, const gg_bf16*
         if (trans_a) ok = encode_map_2d(&mA[q], Xs[src], ms[src], k, ms[src], 64, kBK);
         else ok = encode_map_2d(&mA[q], Xs[src], k, ms[src], k, kBK, kBM);
         if (!ok) return GG_ERR_CUDA;
-        if (trans_b) ok = encode_map_2d(&mB[q], Ws[src], k, ns[src], k, kBK, pair ? kBN / 2 : kBN);
+        if (trans_b) ok = encode_map_2d(&mB[q], Ws[src], k, ns[src], k, kBK, (pair || narrow) ? kBN / 2 : kBN);
         else ok = encode_map_2d(&mB[q], Ws[src], ns[src], k, ns[src], 64, kBK);
         if (!ok) return GG_ERR_CUDA;
     }
     if (!pair) {
+        const int64_t tiles = narrow ? narrow_tiles : single_tiles;
         if (trans_a && trans_b)
-            return launch_gemm<KIND_DUAL, true, false, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, single_tiles, st);
+            return launch_gemm<KIND_DUAL, true, false, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, tiles, st);
         if (trans_a)
-            return launch_gemm<KIND_DUAL, true, true, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, single_tiles, st);
+            return launch_gemm<KIND_DUAL, true, true, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, tiles, st);
         if (trans_b)
-            return launch_gemm<KIND_DUAL, false, false, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, single_tiles, st);
-        return launch_gemm<KIND_DUAL, false, true, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, single_tiles, st);
+            return launch_gemm<KIND_DUAL, false, false, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, tiles, st);
+        return launch_gemm<KIND_DUAL, false, true, false, false, false>(mA[0], mB[0], mA[1], mB[1], p, tiles, st);
     }
     // pair units: two m-tiles of one problem and one n-tile
     const int64_t bound = ((m0 + 2 * kBM - 1) / (2 * kBM)) * ((n0 + kBN - 1) / kBN) +

@@ -51,7 +51,6 @@ constexpr int kMaxStages = 6;
 constexpr int kKRowBytes = kBK * 2;
 constexpr int kKChunks = kKRowBytes / 16;  // 16-byte chunks per K-major row
 constexpr int kABytes = kBM * kBK * 2;
-constexpr int kTmemCols = 2 * kBN;      // two fp32 accumulators
 constexpr int kGroupM = 16;             // m-tiles per raster group (L2 reuse)
 constexpr int kGatherWarps = 4;
 constexpr int kTQ = 8;                  // tile-queue entries (dynamic schedule)
@@ -119,6 +118,9 @@ struct GemmParams {
     // counters {tiles handed out past the first wave, pairs finished}, zero at
     // launch and reset to zero by the last pair to finish
     uint32_t* sched;
+    // dual problems that fit one wave of SMs in 128 x 128 tiles run them (single
+    // CTAs): twice the tiles of 128 x 256, so more SMs share the work
+    int narrow;
     int32_t* status;
 };
 
@@ -178,7 +180,8 @@ static std::atomic<uint32_t> g_sched_next[64];
 // together, CTA rank r taking m-tile 2*unit + r.  A rank whose m-tile falls
 // past the end gets rows <= 0 (a phantom tile: it still loads its operand
 // boxes, its accumulator rows are computed and handed back, nothing is stored).
-template <int KIND, bool PAIR>
+// TN: output columns of a tile (dual problems in narrow single-CTA tiles: kBN / 2)
+template <int KIND, bool PAIR, int TN = kBN>
 __device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
                                                 const int32_t* s_off, const int32_t* s_tp,
                                                 uint32_t rank) {
@@ -243,7 +246,7 @@ __device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
         ti.red_len = s_off[e + 1] - s_off[e];
     } else {
         const int ut0 = ((p.dual[0].m + kBM - 1) / kBM + U - 1) / U;
-        const int64_t tiles0 = static_cast<int64_t>(ut0) * ((p.dual[0].n + kBN - 1) / kBN);
+        const int64_t tiles0 = static_cast<int64_t>(ut0) * ((p.dual[0].n + TN - 1) / TN);
         const int q = t < tiles0 ? 0 : 1;
         const int64_t lt = q == 0 ? t : t - tiles0;
         const int utq = ((p.dual[q].m + kBM - 1) / kBM + U - 1) / U;
@@ -252,7 +255,7 @@ __device__ __forceinline__ TileInfo decode_tile(int64_t t, const GemmParams& p,
         ti.e = q;
         ti.row0 = static_cast<int64_t>(mt) * kBM;
         ti.rows = min(kBM, p.dual[q].m - mt * kBM);
-        ti.n0 = nt * kBN;
+        ti.n0 = nt * TN;
         ti.red0 = 0;
         ti.red_len = p.Kred;
     }
@@ -281,21 +284,25 @@ __device__ __forceinline__ int64_t gather_row(const GemmParams& p, const GatherS
     return r;
 }
 
-template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR>
+// NARROW: single-CTA dual tiles of 128 x 128 (kBN / 2 output columns).
+template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR, bool NARROW = false>
 struct GemmTraits {
     static_assert(!(PAIR && (A_GATHER || B_GATHER)), "2-CTA tiles are loaded by TMA only");
+    static_assert(!NARROW || (!PAIR && KIND == KIND_DUAL), "narrow tiles: single-CTA dual problems");
+    static constexpr int kTileN = NARROW ? kBN / 2 : kBN;  // output columns of a tile
+    static constexpr int kTmemCols = 2 * kTileN;           // two fp32 accumulators
     static constexpr bool kAnyGather = A_GATHER || B_GATHER;
     static constexpr bool kCpGatherFence = kAnyGather;  // cp.async-written stages
     static constexpr int kThreads = 32 * (6 + (kAnyGather ? kGatherWarps : 0) + (PAIR && KIND == KIND_RAGGED_K ? 1 : 0));
     // PAIR dW: a five-stage ring plus one buffer for each tile's ragged tail
     // block, which is loaded a few stages into the tile and consumed last
     // (its rows past the expert's end are zeroed meanwhile).
-    static constexpr int kStages = PAIR ? (KIND == KIND_RAGGED_K ? 5 : 6) : 4;
+    static constexpr int kStages = PAIR ? (KIND == KIND_RAGGED_K ? 5 : 6) : (NARROW ? 6 : 4);
     static constexpr int kBufStages = kStages + (PAIR && KIND == KIND_RAGGED_K ? 1 : 0);
-    static constexpr int kBRows = PAIR ? kBN / 2 : kBN;  // B tile rows (n) held by one CTA
+    static constexpr int kBRows = PAIR ? kBN / 2 : kTileN;  // B tile rows (n) held by one CTA
     static constexpr uint32_t kBBytes = kBRows * kBK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, kBN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, kTileN, A_MN ? 1 : 0, B_MN ? 1 : 0);
     static constexpr uint32_t kTmaBytes = (A_GATHER ? 0u : kABytes) + (B_GATHER ? 0u : kBBytes);
     static constexpr uint32_t kFullCount = 1 + (kAnyGather ? kGatherWarps * 32 : 0);
     // PAIR: both CTAs' TMA bytes of a stage complete on the even CTA's barrier,
@@ -319,6 +326,8 @@ struct GemmTraits {
     // dW tail helper); odd CTA: producer, 4 epilogue warps (+ the tail helper)
     static constexpr int kTqReaders = 10 + (kTailBuf ? 2 : 0);
     static_assert(kStages <= kMaxStages, "stage ring");
+    static_assert(kBufStages * kStageBytes <= (PAIR ? 6u : 4u) * (kABytes + (PAIR ? kBN / 2 : kBN) * kBK * 2),
+                  "ring fits the shared-memory layout");
 };
 
 // per epilogue warp: 32 rows x 128 B of staged output, then the 32 rows' destination pointers
@@ -360,12 +369,13 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t tile_addr, int ks) {
 
 // DYN: the dynamic tile schedule (a separate instantiation, so the static one
 // carries none of its code).
-template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR, bool DYN>
-__global__ void __launch_bounds__((GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>::kThreads), 1)
+template <int KIND, bool A_MN, bool B_MN, bool A_GATHER, bool B_GATHER, bool PAIR, bool DYN, bool NARROW>
+__global__ void __launch_bounds__((GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR, NARROW>::kThreads), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                     const GemmParams p) {
-    using Tr = GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR>;
+    using Tr = GemmTraits<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR, NARROW>;
+    constexpr int TN = Tr::kTileN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -419,10 +429,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     }
     if (warp == 1) {
         if (PAIR) {
-            tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+            tmem_alloc_pair(&ctl->tmem_base, Tr::kTmemCols);
             tmem_relinquish_pair();
         } else {
-            tmem_alloc(&ctl->tmem_base, kTmemCols);
+            tmem_alloc(&ctl->tmem_base, Tr::kTmemCols);
             tmem_relinquish();
         }
     }
@@ -433,8 +443,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         int bad = 0;
         if (KIND == KIND_DUAL) {
             constexpr int U = PAIR ? 2 : 1;
-            const int64_t t0 = static_cast<int64_t>(((p.dual[0].m + kBM - 1) / kBM + U - 1) / U) * ((p.dual[0].n + kBN - 1) / kBN);
-            const int64_t t1 = static_cast<int64_t>(((p.dual[1].m + kBM - 1) / kBM + U - 1) / U) * ((p.dual[1].n + kBN - 1) / kBN);
+            const int64_t t0 = static_cast<int64_t>(((p.dual[0].m + kBM - 1) / kBM + U - 1) / U) * ((p.dual[0].n + TN - 1) / TN);
+            const int64_t t1 = static_cast<int64_t>(((p.dual[1].m + kBM - 1) / kBM + U - 1) / U) * ((p.dual[1].n + TN - 1) / TN);
             total_tiles = t0 + t1;
         } else {
             const int seg = (p.E + 31) / 32;
@@ -675,7 +685,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     ++npub;
                     return true;
                 };
-                const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
+                const TileInfo ti = decode_tile<KIND, PAIR, TN>(t, p, s_off, s_tp, rank);
                 const CUtensorMap* mA = (KIND == KIND_DUAL && ti.e == 1) ? &tmA1 : &tmA0;
                 const CUtensorMap* mB = (KIND == KIND_DUAL && ti.e == 1) ? &tmB1 : &tmB0;
                 // PAIR: one reduction block into (sA, sB), completing on barrier `bar`
@@ -754,7 +764,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                                     tma_load_2d(sB, mB, &ctl->full[stage], red, ti.n0);
                             } else {
 #pragma unroll
-                                for (int cc = 0; cc < kBN / 64; ++cc) {
+                                for (int cc = 0; cc < Tr::kBRows / 64; ++cc) {
                                     if (KIND == KIND_RAGGED_M)
                                         tma_load_3d(sB + cc * kBK * 128, mB, &ctl->full[stage],
                                                     ti.n0 + cc * 64, red, ti.e);
@@ -826,7 +836,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 // the entry may wait for this tile's loads, so the issuer blocks on
                 // it only at the tile's end.)
                 int32_t t = read_tile(0);
-                TileInfo ti_next = t >= 0 ? decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank) : TileInfo{};
+                TileInfo ti_next = t >= 0 ? decode_tile<KIND, PAIR, TN>(t, p, s_off, s_tp, rank) : TileInfo{};
                 int32_t t_next = -1;
                 for (int k = 0; t >= 0 && ok; ++k, t = t_next) {
                     const TileInfo ti = ti_next;
@@ -836,7 +846,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         if (block) t_next = read_tile(k + 1);
                         else if (!try_read_tile(k + 1, t_next)) return;
                         next_decoded = true;
-                        if (t_next >= 0) ti_next = decode_tile<KIND, PAIR>(t_next, p, s_off, s_tp, rank);
+                        if (t_next >= 0) ti_next = decode_tile<KIND, PAIR, TN>(t_next, p, s_off, s_tp, rank);
                     };
                     if (ti.nkb == 0) { decode_next(true); continue; }
                     const uint32_t buf = acc_count & 1u;
@@ -846,7 +856,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + buf * kBN;
+                    const uint32_t d_tmem = tmem_base + buf * TN;
                     // a dW pair's ragged tail block (the last, partly filled one) comes
                     // from the tail buffer after the loop, so the per-stage path carries
                     // no tail test: the issue latency after a stage lands is the
@@ -926,7 +936,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             uint32_t acc_count = 0;
             bool ok = true, any_mma = false;
             for (int64_t t = slot; t < total_tiles; t += nslot) {
-                const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
+                const TileInfo ti = decode_tile<KIND, PAIR, TN>(t, p, s_off, s_tp, rank);
                 if (ti.nkb == 0) continue;
                 const uint32_t buf = acc_count & 1u;
                 const uint32_t acc_phase = (acc_count >> 1) & 1u;
@@ -934,7 +944,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     ok = mbar_wait(&ctl->tmem_empty[buf], acc_phase ^ 1u, abort_flag, p.status, 0, kWaitLimitNs, PAIR);
                     tc_fence_after();
                 }
-                const uint32_t d_tmem = tmem_base + buf * kBN;
+                const uint32_t d_tmem = tmem_base + buf * TN;
                 for (int kb = 0; kb < ti.nkb; ++kb) {
                     if (lane == 0 && ok) ok = mbar_wait(&ctl->full[stage], phase, abort_flag, p.status);
                     const uint32_t sA = stage0 + stage * kStageBytes;
@@ -991,7 +1001,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             }
             // (PAIR: an odd CTA past its expert's last m-tile has rows <= 0; it
             // still takes part in the accumulator hand-off but stores nothing.)
-            const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
+            const TileInfo ti = decode_tile<KIND, PAIR, TN>(t, p, s_off, s_tp, rank);
             const int ncols = tile_cols<KIND>(p, ti.e);
             // destination row, scale, output base
             uint16_t* out = p.out;
@@ -1024,7 +1034,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             uint16_t* arow_out = (KIND == KIND_RAGGED_M && dest >= 0 && p.act_out) ? p.act_out + dest * p.ld_act : nullptr;
             if (ti.nkb == 0) {
                 if (orow) {
-                    for (int c = ti.n0; c < min(ti.n0 + kBN, ncols); c += 8)
+                    for (int c = ti.n0; c < min(ti.n0 + TN, ncols); c += 8)
                         *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
                 }
                 continue;
@@ -1081,7 +1091,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 ++acc_count;
                 continue;
             }
-            const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN;
+            const uint32_t taddr0 = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * TN;
             // convert and store 32 accumulator columns starting at output column col0,
             // straight from registers (16 bytes of the thread's own row per store)
             auto store_out32 = [&](const uint32_t (&v)[32], int col0) {
@@ -1218,7 +1228,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 {
                     const int64_t tn = t + nslot;
                     if (tn < total_tiles) {
-                        const TileInfo tni = decode_tile<KIND, PAIR>(tn, p, s_off, s_tp, rank);
+                        const TileInfo tni = decode_tile<KIND, PAIR, TN>(tn, p, s_off, s_tp, rank);
                         if (r < tni.rows) {
                             const char* hn = reinterpret_cast<const char*>(p.swiglu_h + (tni.row0 + r) * p.ld_h + 2 * tni.n0);
                             const int nbytes = 4 * min(kBN, ncols - tni.n0);  // 2 H values per column
@@ -1268,7 +1278,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             // the last load has landed in registers, before its columns are stored.
             constexpr int kColsPerWait = 128;
 #pragma unroll 1
-            for (int c = 0; c < kBN / kColsPerWait; ++c) {
+            for (int c = 0; c < TN / kColsPerWait; ++c) {
                 uint32_t v0[32], v1[32], v2[32], v3[32];
                 const uint32_t ta = taddr0 + c * kColsPerWait;
                 tmem_ld_32x32b_x32(ta, v0);
@@ -1276,7 +1286,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 tmem_ld_32x32b_x32(ta + 64, v2);
                 tmem_ld_32x32b_x32(ta + 96, v3);
                 tmem_ld_wait();
-                if (c == kBN / kColsPerWait - 1) release_acc();
+                if (c == TN / kColsPerWait - 1) release_acc();
                 const int col0 = ti.n0 + c * kColsPerWait;
                 if (staged) {
                     store_act32(v0, col0);
@@ -1311,7 +1321,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         for (int k = 0;; ++k) {
             const int32_t t = read_tile_warp(k);
             if (t < 0) break;
-            const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
+            const TileInfo ti = decode_tile<KIND, PAIR, TN>(t, p, s_off, s_tp, rank);
             const int nfull = ti.red_len / kBK;
             if (nfull == ti.nkb) continue;
             if (!warp_wait(&ctl->tfull, tail_uses & 1u, abort_flag, p.status)) break;
@@ -1344,7 +1354,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
 #pragma unroll
                 for (int j = 0; j < kARows; ++j) a_next[j] = -1;
                 if (tt < total_tiles) {
-                    const TileInfo tn = decode_tile<KIND, PAIR>(tt, p, s_off, s_tp, rank);
+                    const TileInfo tn = decode_tile<KIND, PAIR, TN>(tt, p, s_off, s_tp, rank);
 #pragma unroll
                     for (int j = 0; j < kARows; ++j) {
                         const int rr = gt / kKChunks + kARowStep * j;
@@ -1382,7 +1392,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             };
             if (A_GATHER && !A_MN) fetch_a_rows(slot);
             for (int64_t t = slot; t < total_tiles && ok; t += nslot) {
-                const TileInfo ti = decode_tile<KIND, PAIR>(t, p, s_off, s_tp, rank);
+                const TileInfo ti = decode_tile<KIND, PAIR, TN>(t, p, s_off, s_tp, rank);
                 const uint16_t* arow[kARows];
                 if (A_GATHER && !A_MN) {
 #pragma unroll
@@ -1469,8 +1479,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     if (PAIR) cluster_sync();  // neither CTA leaves while the other may still signal it
     tc_fence_after();
     if (warp == 1) {
-        if (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
-        else tmem_dealloc(tmem_base, kTmemCols);
+        if (PAIR) tmem_dealloc_pair(tmem_base, Tr::kTmemCols);
+        else tmem_dealloc(tmem_base, Tr::kTmemCols);
     }
 }
 
@@ -1535,13 +1545,15 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
         const uint32_t s = g_sched_next[dev].fetch_add(1u, std::memory_order_relaxed) % kSchedSlots;
         q.sched = static_cast<uint32_t*>(base) + 2 * s;
     }
-    auto kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR, false>;
+    auto kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR, false, false>;
+    int kid = 0;
     if constexpr (Tr::kDynSched)
-        if (q.sched) kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR, true>;
+        if (q.sched) { kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR, true, false>; kid = 1; }
+    if constexpr (KIND == KIND_DUAL && !PAIR)
+        if (p.narrow) { kern = grouped_gemm_kernel<KIND, A_MN, B_MN, A_GATHER, B_GATHER, PAIR, false, true>; kid = 2; }
     // the shared-memory opt-in is set once per kernel and device (host overhead
     // matters for small launches)
-    static std::atomic<bool> smem_set[2][64];
-    const int kid = q.sched ? 1 : 0;
+    static std::atomic<bool> smem_set[3][64];
     if (!smem_set[kid][dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(gemm_smem_bytes<PAIR>(GG_MAX_EXPERTS)));
