@@ -73,12 +73,26 @@ def _peak_value(d, keys, default):
     return default
 
 
+def engine_code_sha():
+    """sha256 of the GEMM engine's code (common.cuh and gemm_engine.cuh with
+    comments and blank lines removed): a comment edit keeps it, any code change
+    does not."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for name in ("common.cuh", "gemm_engine.cuh"):
+        with open(os.path.join(ROOT, "unpermute_route_hist_gb300", "csrc", name)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip()).encode())
+    return h.hexdigest()
+
+
 def _roofline_traffic():
     """Per-launch DRAM bytes of the roofline kernel from the committed ncu
-    summary, or None once the engine source differs from the captured one."""
-    import hashlib
+    summary, or None once the engine's code differs from the captured one."""
     path = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
-    eng = os.path.join(ROOT, "unpermute_route_hist_gb300", "csrc", "gemm_engine.cuh")
     try:
         kv = {}
         with open(path) as fh:
@@ -86,9 +100,7 @@ def _roofline_traffic():
                 if "=" in line and not line.startswith("#"):
                     k, v = (x.strip() for x in line.split("=", 1))
                     kv[k] = v
-        with open(eng, "rb") as fh:
-            sha = hashlib.sha256(fh.read()).hexdigest()
-        if not sha.startswith(kv["engine_sha256_prefix"]):
+        if not engine_code_sha().startswith(kv["engine_code_sha256_prefix"]):
             return None
         return int(kv["dram_bytes_read"]) + int(kv["dram_bytes_write"])
     except Exception:

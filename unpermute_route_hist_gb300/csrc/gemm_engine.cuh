@@ -390,6 +390,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
     const int warp = warp_id(), lane = lane_id();
     volatile int* abort_flag = &ctl->abort_flag;
     // persistent schedule: CTAs (or 2-CTA clusters) take units slot, slot + nslot, ...
+    // (static), or slot and then units handed out by the launch's counter (DYN)
     const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;  // PAIR: the CTA that issues the MMAs
     const int64_t slot = PAIR ? static_cast<int64_t>(cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
@@ -492,8 +493,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                 // bucket, descending.  Chunks of 32 experts are visited in order and
                 // ranked within a chunk by lane, so every CTA computes the same order.
                 // A dW tile's cost grows with its expert's rows; putting the longest
-                // tiles first lets the short ones fill in at the end of the static
-                // round-robin instead of a long tile landing last on one CTA.
+                // tiles first lets the short ones fill in at the end (of the static
+                // round-robin, or of the dynamic hand-out, which then is greedy
+                // longest-first) instead of a long tile landing last on one CTA.
                 __syncwarp();
                 int32_t* cnt = ctl->ord_start;
                 for (int b = lane; b < kOrdBuckets; b += 32) cnt[b] = 0;
