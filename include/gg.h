@@ -117,8 +117,8 @@ int gg_read_status(const int32_t* status, int32_t* code, void* stream);
  * 1024 device counter pairs per launch, in turn, reset by the launch itself
  * as it ends: more than 1023 dynamic launches in flight at once on one
  * device (streams that run concurrently, or replays of one captured graph
- * running concurrently with themselves) is not supported.  No counterpart
- * on the pages. */
+ * running concurrently with themselves) is not supported.  Launches of more
+ * than 2^30 tiles keep the static schedule.  No counterpart on the pages. */
 #define GG_SCHEDULE_AUTO 0
 #define GG_SCHEDULE_STATIC 1
 #define GG_SCHEDULE_DYNAMIC 2

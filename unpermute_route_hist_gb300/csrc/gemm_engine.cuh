@@ -1535,8 +1535,8 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
     const int mode = g_gemm_schedule.load(std::memory_order_relaxed);
     const bool dyn = mode == GG_SCHEDULE_DYNAMIC ||
                      (mode == GG_SCHEDULE_AUTO && mean_blocks >= (KIND == KIND_RAGGED_K ? kDynMinBlocksK : kDynMinBlocksM));
-    if (Tr::kDynSched && dyn) {
-        if (tile_bound > (int64_t(1) << 30)) return GG_ERR_UNSUPPORTED;
+    // (past 2^30 tiles the static schedule, whose tile numbers are 64-bit)
+    if (Tr::kDynSched && dyn && tile_bound <= (int64_t(1) << 30)) {
         static std::atomic<void*> sched_base[64];
         void* base = sched_base[dev].load(std::memory_order_acquire);
         if (!base) {
