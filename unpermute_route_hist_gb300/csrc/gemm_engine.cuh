@@ -1369,7 +1369,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
             // stages before use, then handed to the copying threads by shuffle.
             constexpr int kIPL = kBK / 32;  // slot numbers per lane (1 or 2)
             const int glane = gt & 31;
-            int32_t q_lo[4], q_hi[4];  // look-ahead ring, fully unrolled rotation below
+            int32_t q_lo[4], q_hi[4];  // look-ahead ring: stage kb in entry kb % 4 (below)
             auto load_stage_idx = [&](const TileInfo& tn, int kb, int32_t& lo, int32_t& hi) {
                 const int64_t k0 = static_cast<int64_t>(kb) * kBK + kIPL * glane;
                 lo = (kb < tn.nkb && k0 < tn.red_len) ? p.gather_idx[tn.red0 + k0] : -1;
@@ -1410,17 +1410,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     load_stage_idx(ti, 1, q_lo[1], q_hi[1]);
                     load_stage_idx(ti, 2, q_lo[2], q_hi[2]);
                 }
-                for (int kb = 0; kb < ti.nkb; ++kb) {
-                    if (!warp_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, p.status, 32)) { ok = false; break; }
+                // one reduction block: wait for its stage, gather its rows, arrive when they land
+                auto do_stage = [&](int kb, int32_t cur_lo, int32_t cur_hi) -> bool {
+                    if (!warp_wait(&ctl->empty[stage], phase ^ 1u, abort_flag, p.status, 32)) return false;
                     const uint32_t sA = stage0 + stage * kStageBytes;
                     const uint32_t sB = sA + kABytes;
-                    int32_t cur_lo = 0, cur_hi = 0;
-                    if (kRedGather) {
-                        load_stage_idx(ti, kb + 3, q_lo[3], q_hi[3]);
-                        cur_lo = q_lo[0];
-                        cur_hi = q_hi[0];
-#pragma unroll
-                        for (int j = 0; j < 3; ++j) { q_lo[j] = q_lo[j + 1]; q_hi[j] = q_hi[j + 1]; }
+                    // source rows of this lane's kIPL reduction rows, once a stage; the
+                    // copies below take them by shuffle
+                    int32_t ar_lo = -1, ar_hi = -1, br_lo = -1, br_hi = -1;
+                    if (A_GATHER && A_MN) {
+                        ar_lo = static_cast<int32_t>(src_row(p.ga, cur_lo));
+                        ar_hi = kIPL == 2 ? static_cast<int32_t>(src_row(p.ga, cur_hi)) : -1;
+                    }
+                    if (B_GATHER) {
+                        br_lo = static_cast<int32_t>(src_row(p.gb, cur_lo));
+                        br_hi = kIPL == 2 ? static_cast<int32_t>(src_row(p.gb, cur_hi)) : -1;
                     }
                     if (A_GATHER) {
                         if (!A_MN) {
@@ -1442,8 +1446,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
 #pragma unroll
                             for (int j = 0; j < kBK / 8; ++j) {
                                 const int rr = (gt >> 4) + 8 * j;
-                                const int32_t f = stage_slot(cur_lo, cur_hi, rr);  // every lane shuffles
-                                const int64_t sr = mv ? src_row(p.ga, f) : -1;
+                                const int32_t r = stage_slot(ar_lo, ar_hi, rr);  // every lane shuffles
+                                const int64_t sr = mv ? r : -1;
                                 const uint32_t dst = sA + (pc >> 3) * (kBK * 128) + rr * 128 + (((pc & 7) ^ (rr & 7)) << 4);
                                 cp_async_16(dst, sr >= 0 ? static_cast<const void*>(p.ga.ptr + sr * p.ga.ld + mn) : p.ga.ptr,
                                             sr >= 0 ? 16u : 0u);
@@ -1458,8 +1462,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
 #pragma unroll
                         for (int j = 0; j < kBK / 4; ++j) {
                             const int rr = (gt >> 5) + 4 * j;
-                            const int32_t f = stage_slot(cur_lo, cur_hi, rr);  // every lane shuffles
-                            const int64_t sr = mv ? src_row(p.gb, f) : -1;
+                            const int32_t r = stage_slot(br_lo, br_hi, rr);  // every lane shuffles
+                            const int64_t sr = mv ? r : -1;
                             const uint32_t dst = sB + (pc >> 3) * (kBK * 128) + rr * 128 + (((pc & 7) ^ (rr & 7)) << 4);
                             cp_async_16(dst, sr >= 0 ? static_cast<const void*>(p.gb.ptr + sr * p.gb.ld + mn) : p.gb.ptr,
                                         sr >= 0 ? 16u : 0u);
@@ -1468,6 +1472,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                     // the stage's barrier gets this thread's arrival when its copies land
                     cp_async_mbar_arrive(&ctl->full[stage]);
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    return true;
+                };
+                // The index look-ahead ring: stage kb's slot numbers sit in entry kb % 4,
+                // loaded three stages before.  Four stages an outer step keep every entry
+                // index a compile-time constant, so no register is moved while its load
+                // is in flight (a rotating ring would wait for each new load at once).
+                if constexpr (kRedGather) {
+                    for (int kb0 = 0; kb0 < ti.nkb && ok; kb0 += 4) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int kb = kb0 + u;
+                            if (kb >= ti.nkb) break;
+                            load_stage_idx(ti, kb + 3, q_lo[(u + 3) & 3], q_hi[(u + 3) & 3]);
+                            if (!do_stage(kb, q_lo[u], q_hi[u])) { ok = false; break; }
+                        }
+                    }
+                } else {
+                    for (int kb = 0; kb < ti.nkb; ++kb)
+                        if (!do_stage(kb, 0, 0)) { ok = false; break; }
                 }
             }
             // every copy lands before the CTA can exit
