@@ -569,15 +569,19 @@ def run_gg(args, cfg):
         raise RuntimeError("end-to-end steps on the two buffer sets disagree")
 
     # ---- the same passes with the gather fused into the GEMM (outside the step) -
-    def time_call(fn, reps=3):
+    def time_call(fn, reps=5):
+        # the median of single calls after one warm-up (a mean over back-to-back calls
+        # swung by 20% from run to run with the clocks under the power cap)
         fn()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+        times = []
         for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
             fn()
-        b.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        return statistics.median(times)
 
     rr = o
     # workspaces: the larger dW gather copy (dY2 rows, R x K; X rows are R x K too)
@@ -621,7 +625,7 @@ def run_gg(args, cfg):
             workspace=dw_ws, status=status)), passes["dW1"]),
         "dW1_token_gather_fused_in_loads": (time_call(lambda: gg.backward_dW(
             src["X"], dH, rr["m_sizes"], rr["gather_idx"], T, k, True, False, out=dW1,
-            workspace=False, status=status), reps=1), passes["dW1"]),
+            workspace=False, status=status), reps=3), passes["dW1"]),
     }
     variants = {n: {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12} for n, (ms, fl) in variants.items()}
 
