@@ -334,8 +334,8 @@ int gg_backward_dX_swiglu(const gg_bf16* dY, const gg_bf16* W, const int32_t* m_
  *  gathered operands are first copied into expert order there (X rows
  *  R*K*2 bytes, dY rows R*N*2 bytes) and the reduction reads dense tiles;
  *  with NULL the row gathers are fused into the reduction's operand loads,
- *  which is several times slower on sm_103a (each reduction block needs 64
- *  newly gathered rows).  Both give the same products. */
+ *  which is 2.5-4x slower on sm_103a (each reduction block needs 64 newly
+ *  gathered rows, fetched in 16-byte pieces).  Both give the same products. */
 int gg_backward_dW(const gg_bf16* X, const gg_bf16* dY, const int32_t* m_sizes,
                    const int32_t* gather_idx, int64_t T, int topk, int E, int64_t N, int64_t K,
                    int permute_x, int permute_y, gg_bf16* dW, void* workspace,
