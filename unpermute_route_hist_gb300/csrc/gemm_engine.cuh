@@ -1604,8 +1604,9 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
         // as many 2-CTA clusters as can be resident at once (a GPC with an odd
         // SM count leaves an SM out), at most one per tile pair
         // (the same for both schedules' kernels: same block, registers and shared memory)
-        static int max_clusters[64] = {0};
-        if (max_clusters[dev] == 0) {
+        static std::atomic<int> max_clusters[64];
+        int mc = max_clusters[dev].load(std::memory_order_relaxed);
+        if (mc == 0) {
             cfg.gridDim = dim3(static_cast<unsigned>(sms & ~int64_t(1)));
             int n = 0;
             e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
@@ -1613,9 +1614,10 @@ int launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap&
                 record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidConfiguration);
                 return GG_ERR_CUDA;
             }
-            max_clusters[dev] = n;
+            max_clusters[dev].store(n, std::memory_order_relaxed);
+            mc = n;
         }
-        const int64_t clusters = tile_bound < max_clusters[dev] ? tile_bound : max_clusters[dev];
+        const int64_t clusters = tile_bound < mc ? tile_bound : mc;
         cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
         e = cudaLaunchKernelEx(&cfg, kern, a0, b0, a1, b1, q);
         if (e != cudaSuccess) { record_cuda_error(e); return GG_ERR_CUDA; }
