@@ -21,7 +21,7 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libgg.so")
 
 SOURCES = ["abi.cu", "route.cu", "route_noalloc.cu", "move.cu", "gemm_ragged_m.cu", "gemm_dw.cu", "gemm_dual.cu", "ep.cu"]
-HEADERS = ["common.cuh", "gemm_engine.cuh"]
+HEADERS = ["common.cuh", "gemm_engine.cuh", "gemm_launch.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -11,7 +11,7 @@
 // problem that fits one wave keeps single-CTA tiles, which start ~1 us sooner
 // (the stated 512/256-row shape: 9.8 us against 10.8 us on pairs), and one that
 // fits a wave even in 128 x 128 tiles runs those, over twice as many SMs.
-#include "gemm_engine.cuh"
+#include "gemm_launch.cuh"
 
 using namespace gg;
 

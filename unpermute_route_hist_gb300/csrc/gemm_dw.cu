@@ -8,7 +8,7 @@
 // runs on the dense 2-CTA path: every reduction block of a gathered operand
 // needs 64 newly gathered rows, which cp.async fetches far slower than TMA
 // streams a dense tile.
-#include "gemm_engine.cuh"
+#include "gemm_launch.cuh"
 
 namespace gg {
 int gather_rows_launch(const uint16_t* src, const int32_t* gather_idx, int div, int64_t src_rows,

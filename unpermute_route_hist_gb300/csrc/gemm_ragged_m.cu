@@ -4,7 +4,7 @@
 // fp32 or bf16 atomic adds) and the backward dX (interface.py, grouped_gemm_forward
 // and grouped_gemm_dX), also with the SwiGLU backward fused into its epilogue.  Both run the persistent tcgen05
 // engine of gemm_engine.cuh over the expert-order row tiles.
-#include "gemm_engine.cuh"
+#include "gemm_launch.cuh"
 
 namespace gg {
 int combine_launch(const uint16_t* Y, const int32_t* row_id_map, const float* topk_w, int64_t T,
